@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA attention forward hot path on GB300.
+
+One step = one causal prefill over S=32768 tokens plus one decode of a single
+token against a KV cache of L=65536 positions (the largest prefill and decode
+sizes of the chowfi/kernels README "Result" table), batch 1, 32 query / 8 KV
+heads, head dim 128, bf16 in/out, fp32 accumulate, synthetic seeded N(0,1)
+inputs.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this path
+has) on the host cores, on a bounded sample of the same workload.
+For N > 1 (torchrun, one rank per GPU) every rank runs an independent replica
+of the step ("replicas only": the path needs no exchange between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+S_PREFILL = 32768
+L_DECODE = 65536
+HQ, HKV, D = 32, 8, 128
+METRIC = "GQA attn fwd: prefill TFLOP/s, decode HBM GB/s, % of GB300 roofline"
+WORKLOAD = ("causal prefill S=32768 + decode L=65536, batch 1, 32 q / 8 KV heads, "
+            "D=128, bf16, N(0,1) seeds q=1 k=2 v=3")
+
+# The pages' RTX 5090 numbers for the two halves of the step (context only).
+PAGES_PREFILL_32K_MS = 38.816
+PAGES_DECODE_64K_MS = 0.176
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NORTH_STAR_HBM_GBS = 8000.0
+
+
+def prefill_flops(S: int) -> float:
+    """Causal prefill FLOPs as the target metric counts them: 2*S^2*H*D."""
+    return 2.0 * S * S * HQ * D
+
+
+def decode_flops(L: int) -> float:
+    return 4.0 * HQ * D * L
+
+
+def decode_bytes(L: int) -> float:
+    """K and V caches once, plus q and out: 2*L*8*128*2 + 2*(32*128*2)."""
+    return 2.0 * L * HKV * D * 2 + 2 * HQ * D * 2
+
+
+def step_flops() -> float:
+    return prefill_flops(S_PREFILL) + decode_flops(L_DECODE)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gqa_flash_attention_causal_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch recorded from an ncu capture in
+    profiles/traffic.json, or None if absent or taken on other sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while
+    the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        smax = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        power = [num(r[2]) for r in rows if num(r[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- oracle
+def oracle_sample(seconds: float = 12.0):
+    """Time the fp64 CPU oracle on a bounded sample of the step: every query
+    row of the S=32768 prefill costs 4*H*D*(i+1) flops; rows are drawn evenly
+    over the sequence until about `seconds` of work, plus one full decode at
+    L=65536.  Returns (TFLOP/s, cores, description)."""
+    import numpy as np
+    import oracle
+    from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
+
+    q, k, v = prefill_inputs(S_PREFILL)
+    dq, kc, vc = decode_inputs(L_DECODE)
+    cores = oracle.max_threads()
+
+    def row_flops(rows):
+        return sum(4.0 * HQ * D * (r + 1) for r in rows)
+
+    # calibrate on a few rows, then size the sample
+    probe = list(np.linspace(0, S_PREFILL - 1, 2 * cores).astype(int))
+    t0 = time.perf_counter()
+    oracle.prefill_rows(q, k, v, probe, causal=True)
+    t_probe = time.perf_counter() - t0
+    rate = row_flops(probe) / max(t_probe, 1e-6)
+    n_rows = int(min(S_PREFILL, max(2 * cores, seconds * rate / (4.0 * HQ * D * S_PREFILL / 2))))
+    rows = list(np.linspace(0, S_PREFILL - 1, n_rows).astype(int))
+    t0 = time.perf_counter()
+    oracle.prefill_rows(q, k, v, rows, causal=True)
+    t_pre = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.decode(dq, kc, vc)
+    t_dec = time.perf_counter() - t0
+    flops = row_flops(rows) + decode_flops(L_DECODE)
+    desc = (f"{n_rows} of {S_PREFILL} causal prefill query rows (all 32 heads, evenly spaced) "
+            f"+ one full decode at L={L_DECODE}; fp64 C oracle, OpenMP over (row, head); "
+            f"prefill {t_pre:.2f} s, decode {t_dec:.2f} s")
+    return flops / (t_pre + t_dec) / 1e12, cores, desc, t_pre + t_dec
+
+
+# ----------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms: float, local_units: float, world: int):
+    """Whole-job time = max over ranks, work = sum over ranks (torch.distributed
+    must be initialised when world > 1)."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    samples = []
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state worth burning in beyond the first call
+    per_step = []
+    desc = ""
+    cores = 0
+    for _ in range(args.steps):
+        tf, cores, desc, secs = oracle_sample(seconds=args.ref_seconds)
+        samples.append(tf)
+        per_step.append(secs)
+    value = statistics.median(samples)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import gqa_flash_attention_causal_gb300 as gqa
+    from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gqa.lib()
+    peaks, peaks_src = load_peaks()
+
+    q, k, v = prefill_inputs(S_PREFILL)
+    dq, kc, vc = decode_inputs(L_DECODE)
+    d_q, d_k, d_v = q.to(dev), k.to(dev), v.to(dev)
+    d_dq, d_kc, d_vc = dq.to(dev), kc.to(dev), vc.to(dev)
+    out = torch.empty_like(d_q)
+    dout = torch.empty_like(d_dq)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gqa.prefill(d_q, d_k, d_v, causal=True, out=out)
+        gqa.decode(d_dq, d_kc, d_vc, out=dout)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if gqa.device_error() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    # ------------------------------------------------ timed region (device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            gqa.prefill(d_q, d_k, d_v, causal=True, out=out)
+            ev[i][1].record(stream)
+            gqa.decode(d_dq, d_kc, d_vc, out=dout)
+            ev[i][2].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(stop)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if gqa.device_error() != 0:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    launches = args.steps * (gqa.launches_per_call(False) + gqa.launches_per_call(True))
+
+    ms_step_local = total_ms / args.steps
+    ms_step, flops_all = aggregate(ms_step_local, step_flops() * args.steps, world)
+    value = flops_all / (ms_step * args.steps * 1e-3) / 1e12
+
+    pre_avg = statistics.mean(pre_ms)
+    dec_avg = statistics.mean(dec_ms)
+    pre_tflops = prefill_flops(S_PREFILL) / (pre_avg * 1e-3) / 1e12
+    dec_gbs = decode_bytes(L_DECODE) / (dec_avg * 1e-3) / 1e9
+    peak_tc = peaks["bf16_tflops_sustained"]
+
+    # ------------------------------------------------ end to end (host buffers)
+    h_q, h_k, h_v = (t.pin_memory() for t in (q, k, v))
+    h_dq, h_kc, h_vc = (t.pin_memory() for t in (dq, kc, vc))
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_dout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_dq, h_kc, h_vc))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dout))
+
+    def e2e_step():
+        for dst, src in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_dq, h_dq), (d_kc, h_kc),
+                         (d_vc, h_vc)):
+            dst.copy_(src, non_blocking=True)
+        gqa.prefill(d_q, d_k, d_v, causal=True, out=out)
+        gqa.decode(d_dq, d_kc, d_vc, out=dout)
+        h_out.copy_(out, non_blocking=True)
+        h_dout.copy_(dout, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms_local = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms, e2e_flops = aggregate(e2e_ms_local, step_flops(), world)
+    e2e_value = e2e_flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return None
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, cores, desc, _ = oracle_sample(seconds=args.ref_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    clk = clocks.summary()
+    traffic = profiled_traffic("prefill")
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "global_batch": 1 * world,
+            "seq_len": S_PREFILL,
+            "kv_len": L_DECODE,
+            "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2 (prefill q 256 MiB + k,v 128 MiB; decode KV 256 MiB)",
+        },
+        "roofline": {
+            "kernel": "prefill_kernel",
+            "bound": "tensor",
+            "achieved": pre_tflops,
+            "peak": peak_tc,
+            "unit": "TFLOP/s",
+            "frac": pre_tflops / peak_tc,
+            "traffic": traffic,
+            "peak_kind": f"bf16 sustained ({peaks_src})",
+            "frac_of_burst": pre_tflops / peaks["bf16_tflops"],
+        },
+        "prefill": {
+            "S": S_PREFILL, "ms": pre_avg, "ms_min": min(pre_ms), "tflops": pre_tflops,
+            "frac_of_sustained": pre_tflops / peak_tc,
+            "frac_of_burst": pre_tflops / peaks["bf16_tflops"],
+            "pages_rtx5090_ms": PAGES_PREFILL_32K_MS,
+        },
+        "decode": {
+            "L": L_DECODE, "ms": dec_avg, "ms_min": min(dec_ms), "gbs": dec_gbs,
+            "bound": "hbm", "frac_of_measured_hbm": dec_gbs / peaks["hbm_gbs"],
+            "frac_of_8tbs": dec_gbs / NORTH_STAR_HBM_GBS,
+            "n_split": gqa.decode_num_splits(L_DECODE),
+            "pages_rtx5090_ms": PAGES_DECODE_64K_MS,
+        },
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-seconds", type=float, default=12.0,
+                    help="CPU seconds of oracle work per reference step / baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+            world = 1
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    try:
+        line = run_reference(args, world, rank) if args.impl == "reference" else \
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+"""GB300 (sm_103a) grouped-query attention forward: Python binding.
+
+The compute lives entirely in ``libgqa_attn.so`` (hand-written CUDA behind
+the C ABI of ``include/gqa_attn.h``); this module only checks and marshals
+torch tensors (device pointers, the current CUDA stream) and turns status
+codes into exceptions.  There is no fallback: if the library is missing or
+the device is not a GB300, every call raises.
+
+Geometry (chowfi/kernels README, "Result" section): batch 1, 32 query heads
+sharing 8 KV heads, head dim 128, bf16, sequence-major BSHD tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .inputs import HEAD_DIM, HKV, HQ
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgqa_attn.so")
+
+STATUS = {
+    0: "GQA_OK", 1: "GQA_ERR_NULL", 2: "GQA_ERR_ALIGN", 3: "GQA_ERR_SHAPE",
+    4: "GQA_ERR_DEVICE", 5: "GQA_ERR_WORKSPACE", 6: "GQA_ERR_TIMEOUT",
+    7: "GQA_ERR_CUDA", 8: "GQA_ERR_POINTER",
+}
+
+# Every symbol include/gqa_attn.h declares, with its ctypes signature.
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _P]),
+    "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
+    "gqa_attn_decode_workspace_bytes": (_S, [_I]),
+    "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
+    "gqa_attn_decode_num_splits": (_I, [_I]),
+    "gqa_attn_launches_per_call": (_I, [_I]),
+    "gqa_attn_device_error": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
+    "gqa_attn_status_string": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+class GqaError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        msg = lib().gqa_attn_status_string(code).decode()
+        super().__init__(f"{fn}: {STATUS.get(code, code)} ({msg})")
+
+
+def lib():
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype, f.argtypes = res, args
+        _lib = l
+    return _lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise GqaError(fn, code)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _expect(t, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bf16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill(q, k, v, causal: bool = True, out=None, stream=None):
+    """Attention over a whole prompt: q [1,S,32,128], k/v [1,S,8,128] bf16.
+
+    Returns ``out`` [1,S,32,128] bf16 (allocated if not given), enqueued on
+    ``stream`` (default: torch's current stream).
+    """
+    import torch
+    S = q.shape[1]
+    _expect(q, (1, S, HQ, HEAD_DIM), "q")
+    _expect(k, (1, S, HKV, HEAD_DIM), "k")
+    _expect(v, (1, S, HKV, HEAD_DIM), "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, (1, S, HQ, HEAD_DIM), "out")
+    _check("gqa_attn_prefill", lib().gqa_attn_prefill(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S,
+        1 if causal else 0, _stream(stream)))
+    return out
+
+
+def decode(q, kcache, vcache, out=None, workspace=None, stream=None):
+    """One query token q [1,1,32,128] against kcache/vcache [1,L,8,128] bf16.
+
+    With ``workspace`` (a CUDA tensor of at least ``decode_workspace_bytes(L)``
+    bytes) the caller-workspace entry point is used; otherwise the library's
+    own per-device workspace.
+    """
+    import torch
+    L = kcache.shape[1]
+    _expect(q, (1, 1, HQ, HEAD_DIM), "q")
+    _expect(kcache, (1, L, HKV, HEAD_DIM), "kcache")
+    _expect(vcache, (1, L, HKV, HEAD_DIM), "vcache")
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, (1, 1, HQ, HEAD_DIM), "out")
+    s = _stream(stream)
+    if workspace is None:
+        _check("gqa_attn_decode", lib().gqa_attn_decode(
+            q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(), L, s))
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+        _check("gqa_attn_decode_ws", lib().gqa_attn_decode_ws(
+            q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(), L,
+            workspace.data_ptr(), nbytes, s))
+    return out
+
+
+def decode_workspace_bytes(L: int) -> int:
+    return int(lib().gqa_attn_decode_workspace_bytes(int(L)))
+
+
+def decode_num_splits(L: int) -> int:
+    return int(lib().gqa_attn_decode_num_splits(int(L)))
+
+
+def launches_per_call(is_decode: bool) -> int:
+    return int(lib().gqa_attn_launches_per_call(1 if is_decode else 0))
+
+
+def device_error(clear: bool = True) -> int:
+    """Synchronise the device and return its error word (0 = no error)."""
+    word = ctypes.c_uint(0)
+    code = lib().gqa_attn_device_error(ctypes.byref(word), 1 if clear else 0)
+    if code not in (0, 6):
+        raise GqaError("gqa_attn_device_error", code)
+    return int(word.value)

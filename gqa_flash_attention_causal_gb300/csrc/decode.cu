@@ -1,0 +1,326 @@
+// decode.cu -- single-token GQA decode against a KV cache: split-KV kernel
+// plus log-sum-exp combine kernel (sm_103a).
+//
+// What the chowfi/kernels README ("What helped most", items 1, 2 and 5)
+// describes for decode, restated for GB300:
+//  * one decode token is too little work for the GPU, so the KV length is cut
+//    into chunks that run in parallel on every SM and are merged afterwards
+//    (item 1: split-KV);
+//  * the 4 query heads of a group read their shared K/V once, not 4 times
+//    (item 2: GQA packing): one CTA owns (chunk, KV head) and computes all 4
+//    query heads from one pass over that chunk;
+//  * K/V are read exactly once, so their loads carry an L2 evict-first hint
+//    (item 5: cache hints for read-once data);
+//  * softmax in base 2 with log2(e) folded into the score scale (item 5).
+//
+// The work is HBM-bound (4 flops per byte), so the design goal is keeping
+// enough bytes in flight: K/V tiles stream through a 3-stage TMA ring, two
+// CTAs per SM.  The 16-key x 128-dim x 4-head products go through warp-level
+// bf16 MMA (m16n8k16) with fp32 accumulation: one ldmatrix + one MMA replaces
+// 256 scalar FMAs, which keeps instruction issue far below the memory time.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kWarps = 4;                        // compute warps per CTA
+constexpr int kStageKeys = 16 * kWarps;          // 64 keys per stage
+constexpr int kStages = 3;                       // TMA ring depth
+constexpr int kHalfBytes = kStageKeys * 128;     // 64 keys x 64 dims x 2 B
+constexpr int kTileBytes = 2 * kHalfBytes;       // K (or V) tile, 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;      // K + V, 32 KB
+constexpr int kThreads = (kWarps + 1) * 32;      // + one TMA producer warp
+constexpr int kCtasPerSm = 2;
+constexpr int kCmbFloats = kWarps * kGroup * kD; // cross-warp merge buffer
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + size_t(kStages) * kStageBytes +
+                              size_t(kCmbFloats) * 4 + 2 * kWarps * kGroup * 4 +
+                              2 * kStages * 8;
+
+static_assert(kStageKeys == kDecodeBoxRows, "tensor-map box must match a stage");
+
+// log2(e) / sqrt(128): scores are kept in the base-2 domain.
+constexpr float kScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap,
+                    const __nv_bfloat16 *__restrict__ q, int L, int chunk,
+                    float *__restrict__ part_o, float *__restrict__ part_lse,
+                    unsigned *err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *cmb_o = reinterpret_cast<float *>(smem + kStages * kStageBytes);
+    float *cmb_m = cmb_o + kCmbFloats;
+    float *cmb_l = cmb_m + kWarps * kGroup;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cmb_l + kWarps * kGroup);
+    const uint32_t tiles = smem_u32(smem);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+
+    const int split = blockIdx.x, g = blockIdx.y;
+    const int key0 = split * chunk;
+    const int key_end = min(L, key0 + chunk);
+    const int n_iter = (key_end - key0 + kStageKeys - 1) / kStageKeys;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Let the combine kernel (a programmatic dependent) get scheduled now; it
+    // still waits for this whole grid to finish before reading its results.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+            const uint64_t pol = policy_evict_first();
+            for (int it = 0; it < n_iter; ++it) {
+                const int s = it % kStages;
+                if (it >= kStages &&
+                    !mbar_wait(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, err, kErrWaitEmpty))
+                    break;
+                const uint32_t full = full0 + 8 * s, dst = tiles + s * kStageBytes;
+                const int row = key0 + it * kStageKeys;
+                mbar_arrive_expect_tx(full, kStageBytes);
+                tma_load_3d(dst, &kmap, full, 0, g, row, pol);
+                tma_load_3d(dst + kHalfBytes, &kmap, full, 64, g, row, pol);
+                tma_load_3d(dst + kTileBytes, &vmap, full, 0, g, row, pol);
+                tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, full, 64, g, row, pol);
+            }
+        }
+        return;  // the producer takes no part in the merge below
+    }
+
+    // -------------------------------------------------------- compute warps
+    // Mapping (m16n8k16 fragments, gi = lane/4, ti = lane%4):
+    //   S^T[key][head] = K[key][d] . Q^T[d][head]   (A = K via ldmatrix,
+    //   B = the 4 query heads of this group in columns 0..3, 4..7 zero)
+    //   O^T[d][head]  += V^T[d][key] . P^T[key][head]  (A = V^T via
+    //   ldmatrix.trans, B = P^T from the S^T fragment by movmatrix.trans)
+    // A lane owns heads 2ti and 2ti+1 in both products, so the running max,
+    // sum and O rescale stay in registers.
+    const int gi = lane >> 2, ti = lane & 3;
+    uint32_t qf[8][2];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        if (gi < kGroup) {
+            const uint32_t *qh = reinterpret_cast<const uint32_t *>(
+                q + (g * kGroup + gi) * kD + 16 * kk + 2 * ti);
+            qf[kk][0] = __ldg(qh);
+            qf[kk][1] = __ldg(qh + 4);
+        } else {
+            qf[kk][0] = qf[kk][1] = 0u;
+        }
+    }
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int kb = warp * 16;  // this warp's 16 keys inside a stage
+
+    for (int it = 0; it < n_iter; ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(full0 + 8 * s, (it / kStages) & 1, err, kErrWaitFull)) break;
+        const uint32_t kt = tiles + s * kStageBytes, vt = kt + kTileBytes;
+
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+        {
+            const uint32_t row = kb + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sw128(kt + (kk >> 2) * kHalfBytes, row, 2 * (kk & 3) + (lane >> 4)),
+                        a0, a1, a2, a3);
+                mma_bf16_16816(c0, c1, c2, c3, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            }
+        }
+        const int key_a = key0 + it * kStageKeys + kb + gi, key_b = key_a + 8;
+        float x0 = c0 * kScaleLog2, x1 = c1 * kScaleLog2;
+        float x2 = c2 * kScaleLog2, x3 = c3 * kScaleLog2;
+        if (key_a >= L) x0 = x1 = -INFINITY;
+        if (key_b >= L) x2 = x3 = -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float r0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked
+        const float r1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
+        const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1);
+        const float p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+        const uint32_t b0 = movmatrix_t(pack_bf16(p0, p1));  // keys 0..7
+        const uint32_t b1 = movmatrix_t(pack_bf16(p2, p3));  // keys 8..15
+        {
+            const int mi = lane >> 3;
+            const uint32_t row = kb + (lane & 7) + (mi >> 1) * 8;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int dc = 2 * mt + (mi & 1);  // 16-byte chunk along d
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(sw128(vt + (dc >> 3) * kHalfBytes, row, dc & 7), a0, a1, a2, a3);
+                mma_bf16_16816(o[mt][0], o[mt][1], o[mt][2], o[mt][3], a0, a1, a2, a3, b0, b1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+
+    // ------------------------------------------- merge the 4 warps' states
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (ti < 2) {
+        const int h0 = 2 * ti, h1 = 2 * ti + 1;
+        float *w0 = cmb_o + (warp * kGroup + h0) * kD;
+        float *w1 = cmb_o + (warp * kGroup + h1) * kD;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int d = 16 * mt + gi;
+            w0[d] = o[mt][0];
+            w1[d] = o[mt][1];
+            w0[d + 8] = o[mt][2];
+            w1[d + 8] = o[mt][3];
+        }
+        if (gi == 0) {
+            cmb_m[warp * kGroup + h0] = m0;
+            cmb_m[warp * kGroup + h1] = m1;
+            cmb_l[warp * kGroup + h0] = l0;
+            cmb_l[warp * kGroup + h1] = l1;
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
+
+    const int t = threadIdx.x;            // 0..127
+    const int n = t >> 5, d0 = (t & 31) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmb_m[w * kGroup + n]);
+    float den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float mw = cmb_m[w * kGroup + n];
+        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+        den += f * cmb_l[w * kGroup + n];
+        const float4 v = *reinterpret_cast<const float4 *>(cmb_o + (w * kGroup + n) * kD + d0);
+        acc[0] += f * v.x;
+        acc[1] += f * v.y;
+        acc[2] += f * v.z;
+        acc[3] += f * v.w;
+    }
+    const float inv = 1.f / den;
+    const int hq = g * kGroup + n;
+    *reinterpret_cast<float4 *>(part_o + (size_t(split) * kHq + hq) * kD + d0) =
+        make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    if (d0 == 0) part_lse[split * kHq + hq] = M + __log2f(den);
+}
+
+// Merge the chunk results of every query head: with per-chunk normalised
+// outputs O_c and log2-sum-exp values lse_c,
+//   out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M),  M = max_c lse_c.
+__global__ void __launch_bounds__(kD)
+decode_combine_kernel(const float *__restrict__ part_o,
+                      const float *__restrict__ part_lse, int n_split,
+                      __nv_bfloat16 *__restrict__ out) {
+    // Launched as a programmatic dependent of the split kernel: wait until
+    // its results are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int h = blockIdx.x, d = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_lse[s * kHq + h]);
+    float num = 0.f, den = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < n_split; ++s) {
+        const float w = ex2(part_lse[s * kHq + h] - M);
+        den += w;
+        num += w * part_o[(size_t(s) * kHq + h) * kD + d];
+    }
+    out[h * kD + d] = __float2bfloat16_rn(num / den);
+}
+
+}  // namespace
+
+DecodePlan decode_plan(int L, int num_sms) {
+    const int max_split = (L + kStageKeys - 1) / kStageKeys;
+    int n = num_sms * kCtasPerSm / kHkv;  // one wave of (split, head) CTAs
+    if (n < 1) n = 1;
+    if (n > max_split) n = max_split;
+    int chunk = (L + n - 1) / n;
+    chunk = (chunk + kStageKeys - 1) / kStageKeys * kStageKeys;
+    DecodePlan p;
+    p.chunk = chunk;
+    p.n_split = (L + chunk - 1) / chunk;
+    return p;
+}
+
+size_t decode_workspace_bytes(const DecodePlan &p) {
+    const size_t o = size_t(p.n_split) * kHq * kD * sizeof(float);
+    const size_t lse = size_t(p.n_split) * kHq * sizeof(float);
+    return o + ((lse + 255) / 256) * 256;
+}
+
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          const void *q, void *out, int L, const DecodePlan &plan,
+                          void *workspace, unsigned *err, cudaStream_t stream) {
+    static bool configured[kMaxDevices] = {};  // the attribute is per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
+        e = cudaFuncSetAttribute(decode_split_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    float *part_o = static_cast<float *>(workspace);
+    float *part_lse = part_o + size_t(plan.n_split) * kHq * kD;
+
+    decode_split_kernel<<<dim3(plan.n_split, kHkv), kThreads, kSmemBytes, stream>>>(
+        kmap, vmap, static_cast<const __nv_bfloat16 *>(q), L, plan.chunk, part_o, part_lse,
+        err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kHq);
+    cfg.blockDim = dim3(kD);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel,
+                              static_cast<const float *>(part_o),
+                              static_cast<const float *>(part_lse), plan.n_split,
+                              static_cast<__nv_bfloat16 *>(out));
+}
+
+}  // namespace gqa

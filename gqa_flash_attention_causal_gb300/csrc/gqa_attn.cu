@@ -1,0 +1,277 @@
+// gqa_attn.cu -- host side of the C ABI declared in include/gqa_attn.h:
+// argument validation, per-device state (SM count, error word, decode
+// workspace), TMA tensor-map encoding and kernel dispatch.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gqa_attn.h"
+#include "internal.h"
+
+using gqa::kD;
+using gqa::kHkv;
+using gqa::kHq;
+using gqa::kMaxDevices;
+
+namespace {
+
+// Per-device word the kernels OR their error bits into (bounded waits that
+// ran out).  Read and cleared through gqa_attn_device_error().
+__device__ unsigned g_device_error;
+
+constexpr int kMaxPrefillLen = 1 << 20;
+constexpr int kMaxDecodeLen = 1 << 26;
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned *err = nullptr;       // device address of g_device_error
+    void *workspace = nullptr;     // decode partials (library-owned)
+    size_t workspace_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Current device's state, probing it on first use.
+gqa_status current_device(DeviceState **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GQA_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return GQA_ERR_CUDA;
+        }
+        d.supported = (major == 10 && minor == 3);
+        if (d.supported &&
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_device_error) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return GQA_ERR_CUDA;
+        }
+        d.probed = true;
+    }
+    if (!d.supported) return GQA_ERR_DEVICE;
+    *out = &d;
+    return GQA_OK;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// Device memory of the current device (plain or managed)?
+gqa_status check_device_ptr(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_POINTER;
+    }
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (a.type == cudaMemoryTypeDevice && a.device == dev) return GQA_OK;
+    if (a.type == cudaMemoryTypeManaged) return GQA_OK;
+    return GQA_ERR_POINTER;
+}
+
+// [rows][heads][128] bf16 tensor, boxes of box_rows x 1 head x 64 dims,
+// 128-byte swizzle (the layout the kernels' shared-memory tiles assume).
+gqa_status encode_bshd(CUtensorMap *m, const void *base, int rows, int heads, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return GQA_ERR_CUDA;
+    const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(heads), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(heads) * kD * 2};
+    const cuuint32_t box[3] = {64u, 1u, cuuint32_t(box_rows)};
+    const cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return GQA_OK;
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+}
+
+// Validation shared by both decode entry points; launches nothing.
+gqa_status decode_args(const void *q, const void *kc, const void *vc, void *out, int L,
+                       DeviceState **dev) {
+    if (!q || !kc || !vc || !out) return GQA_ERR_NULL;
+    if (misaligned(q) || misaligned(kc) || misaligned(vc) || misaligned(out))
+        return GQA_ERR_ALIGN;
+    if (L < 1 || L > kMaxDecodeLen) return GQA_ERR_SHAPE;
+    gqa_status st = current_device(dev);
+    if (st != GQA_OK) return st;
+    for (const void *p : {q, kc, vc, static_cast<const void *>(out)}) {
+        st = check_device_ptr(p);
+        if (st != GQA_OK) return st;
+    }
+    return GQA_OK;
+}
+
+gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, int L,
+                      const gqa::DecodePlan &plan, void *ws, unsigned *err,
+                      cudaStream_t stream) {
+    CUtensorMap kmap, vmap;
+    gqa_status st = encode_bshd(&kmap, kc, L, kHkv, gqa::kDecodeBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, vc, L, kHkv, gqa::kDecodeBoxRows);
+    if (st != GQA_OK) return st;
+    return from_cuda(gqa::launch_decode(kmap, vmap, q, out, L, plan, ws, err, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *out, int S,
+                            int causal, cudaStream_t stream) {
+    if (!q || !k || !v || !out) return GQA_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
+        return GQA_ERR_ALIGN;
+    if (S < 1 || S > kMaxPrefillLen) return GQA_ERR_SHAPE;
+    DeviceState *dev = nullptr;
+    gqa_status st = current_device(&dev);
+    if (st != GQA_OK) return st;
+    for (const void *p : {q, k, v, static_cast<const void *>(out)}) {
+        st = check_device_ptr(p);
+        if (st != GQA_OK) return st;
+    }
+    CUtensorMap qmap, kmap, vmap;
+    st = encode_bshd(&qmap, q, S, kHq, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&kmap, k, S, kHkv, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, v, S, kHkv, gqa::kPrefillBoxRows);
+    if (st != GQA_OK) return st;
+    return from_cuda(gqa::launch_prefill(qmap, kmap, vmap, out, S, causal ? 1 : 0,
+                                         dev->num_sms, dev->err, stream));
+}
+
+size_t gqa_attn_decode_workspace_bytes(int L) {
+    if (L < 1 || L > kMaxDecodeLen) return 0;
+    DeviceState *dev = nullptr;
+    if (current_device(&dev) != GQA_OK) return 0;
+    return gqa::decode_workspace_bytes(gqa::decode_plan(L, dev->num_sms));
+}
+
+int gqa_attn_decode_num_splits(int L) {
+    if (L < 1 || L > kMaxDecodeLen) return 0;
+    DeviceState *dev = nullptr;
+    if (current_device(&dev) != GQA_OK) return 0;
+    return gqa::decode_plan(L, dev->num_sms).n_split;
+}
+
+gqa_status gqa_attn_decode_ws(const void *q, const void *kcache, const void *vcache,
+                              void *out, int L, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    DeviceState *dev = nullptr;
+    gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
+    if (st != GQA_OK) return st;
+    const gqa::DecodePlan plan = gqa::decode_plan(L, dev->num_sms);
+    if (!workspace || misaligned(workspace) ||
+        workspace_bytes < gqa::decode_workspace_bytes(plan))
+        return GQA_ERR_WORKSPACE;
+    st = check_device_ptr(workspace);
+    if (st != GQA_OK) return GQA_ERR_WORKSPACE;
+    return run_decode(q, kcache, vcache, out, L, plan, workspace, dev->err, stream);
+}
+
+gqa_status gqa_attn_decode(const void *q, const void *kcache, const void *vcache, void *out,
+                           int L, cudaStream_t stream) {
+    DeviceState *dev = nullptr;
+    gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
+    if (st != GQA_OK) return st;
+    const gqa::DecodePlan plan = gqa::decode_plan(L, dev->num_sms);
+    const size_t need = gqa::decode_workspace_bytes(plan);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (dev->workspace_bytes < need) {
+            // Size for the largest plan this device can produce, once.
+            const gqa::DecodePlan most = gqa::decode_plan(kMaxDecodeLen, dev->num_sms);
+            size_t bytes = gqa::decode_workspace_bytes(most);
+            if (bytes < need) bytes = need;
+            void *p = nullptr;
+            if (cudaMalloc(&p, bytes) != cudaSuccess) {
+                cudaGetLastError();
+                return GQA_ERR_CUDA;
+            }
+            if (dev->workspace) cudaFree(dev->workspace);
+            dev->workspace = p;
+            dev->workspace_bytes = bytes;
+        }
+    }
+    return run_decode(q, kcache, vcache, out, L, plan, dev->workspace, dev->err, stream);
+}
+
+int gqa_attn_launches_per_call(int is_decode) { return is_decode ? 2 : 1; }
+
+gqa_status gqa_attn_device_error(unsigned int *flags, int clear) {
+    if (!flags) return GQA_ERR_NULL;
+    DeviceState *dev = nullptr;
+    gqa_status st = current_device(&dev);
+    if (st != GQA_OK) return st;
+    unsigned word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, dev->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    if (clear && word) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(dev->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            return GQA_ERR_CUDA;
+        }
+    }
+    *flags = word;
+    return word ? GQA_ERR_TIMEOUT : GQA_OK;
+}
+
+const char *gqa_attn_status_string(gqa_status s) {
+    switch (s) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_NULL: return "a required pointer is NULL";
+    case GQA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case GQA_ERR_SHAPE: return "sequence length out of range";
+    case GQA_ERR_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case GQA_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
+    case GQA_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case GQA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case GQA_ERR_POINTER: return "a pointer is not device memory of the current device";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// internal.h -- declarations shared by the host C-ABI layer and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+constexpr int kHq = 32;    // query heads
+constexpr int kHkv = 8;    // KV heads
+constexpr int kGroup = 4;  // query heads per KV head
+constexpr int kD = 128;    // head dim
+constexpr int kMaxDevices = 64;
+
+// ------------------------------------------------------------------ decode
+// Split plan: the KV length is cut into n_split chunks of `chunk` keys (a
+// multiple of the 64-key stage); CTA (split, g) handles chunk `split` of KV
+// head g for its 4 query heads.
+struct DecodePlan {
+    int n_split;
+    int chunk;
+};
+DecodePlan decode_plan(int L, int num_sms);
+size_t decode_workspace_bytes(const DecodePlan &p);
+
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          const void *q, void *out, int L, const DecodePlan &plan,
+                          void *workspace, unsigned *err, cudaStream_t stream);
+
+// Box sizes the kernels expect in their tensor maps (rows of 64 bf16 each).
+constexpr int kDecodeBoxRows = 64;
+constexpr int kPrefillBoxRows = 128;
+
+// ------------------------------------------------------------------ prefill
+cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, void *out, int S, int causal,
+                           int num_sms, unsigned *err, cudaStream_t stream);
+
+}  // namespace gqa

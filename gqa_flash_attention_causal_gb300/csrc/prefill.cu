@@ -1,0 +1,466 @@
+// prefill.cu -- causal (or bidirectional) GQA prefill attention on sm_103a:
+// TMA-staged tiles, tcgen05 MMA with fp32 accumulators in TMEM, online
+// softmax in registers, causal tile skipping and a persistent
+// longest-first schedule.
+//
+// Mapping of the chowfi/kernels README ("What helped most") onto GB300:
+//  * item 3, skip the masked half: a query tile only visits KV tiles up to
+//    and including its diagonal tile; only the diagonal tile is masked;
+//  * item 4, largest blocks first: work items are ordered by their number of
+//    KV tiles, descending, and dealt to persistent CTAs (one per SM) in a
+//    snake order so every CTA ends with the short items;
+//  * item 5, exp2 softmax: log2(e)/sqrt(128) is folded into one FFMA per score
+//    ahead of the MUFU ex2;
+//  * item 2, GQA: the 4 query heads of a KV group are adjacent in the item
+//    order, so their K/V tiles are L2 hits for one another.
+//
+// One work item = one query head x 256 query rows, held as two 128-row Q
+// tiles (A and B) that share every K/V tile loaded into shared memory.
+// Roles (320 threads):
+//   warps 0-3  softmax of tile A (thread r owns TMEM lane / query row r)
+//   warps 4-7  softmax of tile B
+//   warp  8    TMA producer: Q tiles, then K_j, V_j into a 4-slot ring
+//   warp  9    TMEM allocator and tcgen05.mma issuer (one thread)
+// TMEM (512 columns x 128 lanes, fp32):
+//   S_A [0,128)  S_B [128,256)  O_A [256,384)  O_B [384,512)
+//   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
+// MMA issue order per KV tile j:  PV_A(j), S_A(j+1), PV_B(j), S_B(j+1):
+// while one tile's softmax runs, the tensor core works on the other's.
+// O is rescaled only when a row maximum grows by more than 2^8 (the final
+// O / l uses the same stale maximum, so the result is unchanged).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kBM = 128;                       // query rows per tile
+constexpr int kBN = 128;                       // keys per KV tile
+constexpr int kTiles = 2;                      // Q tiles per work item
+constexpr int kStages = 4;                     // K/V ring slots
+constexpr int kTileBytes = kBM * kD * 2;       // 32 KB
+constexpr int kHalfBytes = kTileBytes / 2;     // [128 rows][64 dims], 16 KB
+constexpr int kSoftmaxWarps = 4 * kTiles;
+constexpr int kWarpLoad = kSoftmaxWarps;       // 8
+constexpr int kWarpMma = kSoftmaxWarps + 1;    // 9
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kQBytes = kTiles * kTileBytes;
+constexpr int kRingBytes = kStages * kTileBytes;
+// q_full, q_empty, kv_full[4], kv_empty[4], s_full[2], p_full[2], o_full[2]
+constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles;
+constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16;
+constexpr uint32_t kTmemCols = 512;
+
+static_assert(kBM == kPrefillBoxRows && kBN == kPrefillBoxRows, "tensor-map box");
+
+constexpr uint32_t kIdescS = umma_idesc_bf16(kBM, kBN, 0, 0);  // Q.K^T, both K-major
+constexpr uint32_t kIdescO = umma_idesc_bf16(kBM, kD, 0, 1);   // P.V, V MN-major
+constexpr float kScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
+constexpr float kRescaleLog2 = 8.0f;
+
+struct Bars {
+    uint32_t base;
+    __device__ uint32_t q_full() const { return base; }
+    __device__ uint32_t q_empty() const { return base + 8; }
+    __device__ uint32_t kv_full(int s) const { return base + 16 + 8 * s; }
+    __device__ uint32_t kv_empty(int s) const { return base + 16 + 8 * kStages + 8 * s; }
+    __device__ uint32_t s_full(int t) const { return base + 16 + 16 * kStages + 8 * t; }
+    __device__ uint32_t p_full(int t) const { return base + 32 + 16 * kStages + 8 * t; }
+    __device__ uint32_t o_full(int t) const { return base + 48 + 16 * kStages + 8 * t; }
+};
+
+// Work decomposition shared by every role: item idx -> (block b, head h),
+// blocks with the most KV tiles first, the 4 heads of a KV group adjacent.
+struct Work {
+    int S, T, n_blocks, n_items, causal;
+    __device__ Work(int S_, int causal_) : S(S_), causal(causal_) {
+        T = (S + kBM - 1) / kBM;
+        n_blocks = (T + 1) / 2;
+        n_items = n_blocks * kHq;
+    }
+    // Item of round `r` for CTA `c` (snake order over the grid).
+    __device__ int item(int r, int c, int G) const {
+        return r * G + ((r & 1) ? (G - 1 - c) : c);
+    }
+    __device__ void coords(int idx, int &b, int &h) const {
+        b = causal ? n_blocks - 1 - idx / kHq : idx / kHq;
+        h = idx % kHq;
+    }
+    // KV tiles visited by tile t (0 = A, 1 = B) of block b.
+    __device__ int n_kv(int b, int t) const {
+        if (!causal) return T;
+        const int n = 2 * b + t + 1;
+        return n < T ? n : T;
+    }
+};
+
+// Bounded wait shared by a whole warp: every lane polls; if any lane gives up
+// (timeout or another role's abort) the warp gives up together.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned *err,
+                                          unsigned code, volatile int *abort) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const long long t0 = clock64();
+        while (!(ok = mbar_try_wait(bar, parity))) {
+            if (*abort || clock64() - t0 > kWaitLimitCycles) break;
+        }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+        if ((threadIdx.x & 31) == 0) {
+            atomicOr(err, code);
+            *abort = 1;
+        }
+    }
+    return ok;
+}
+// Same for a single thread (producer / MMA issuer).
+__device__ __forceinline__ bool lone_wait(uint32_t bar, uint32_t parity, unsigned *err,
+                                          unsigned code, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort || clock64() - t0 > kWaitLimitCycles) {
+            atomicOr(err, code);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    // 16-dim K step kk of a [128 rows][128 dims] tile stored as two swizzled
+    // [128][64] halves: 32-byte steps inside a half, 8-row groups 1 KB apart.
+    return umma_desc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t vdesc(uint32_t tile, int kk) {
+    // V as the MN-major B operand: 16-key step kk = 16 rows of 128 B; the two
+    // 64-dim halves are kHalfBytes apart (LBO), 8-key groups 1 KB apart (SBO).
+    return umma_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+               const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, __nv_bfloat16 *__restrict__ out,
+               int S, int causal, unsigned *err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sRing = sQ + kQBytes;
+    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + kQBytes + kRingBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mem + kNumBars);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const Bars bars{smem_u32(bar_mem)};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Work work(S, causal);
+    const int G = gridDim.x, cta = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.q_full(), 1);
+        mbar_init(bars.q_empty(), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bars.kv_full(s), 1);
+            mbar_init(bars.kv_empty(s), 1);
+        }
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bars.s_full(t), 1);
+            mbar_init(bars.p_full(t), 4);
+            mbar_init(bars.o_full(t), 1);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpLoad) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&qmap);
+            prefetch_tmap(&kmap);
+            prefetch_tmap(&vmap);
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_last();
+            int kv = 0;
+            bool ok = true;
+            for (int r = 0, n = 0; ok; ++r, ++n) {
+                const int idx = work.item(r, cta, G);
+                if (idx >= work.n_items) break;
+                int b, h;
+                work.coords(idx, b, h);
+                const int g = h / kGroup;
+                if (n > 0 && !(ok = lone_wait(bars.q_empty(), (n - 1) & 1, err,
+                                              kErrWaitEmpty, abort)))
+                    break;
+                mbar_arrive_expect_tx(bars.q_full(), kQBytes);
+                for (int t = 0; t < kTiles; ++t) {
+                    const int row = (2 * b + t) * kBM;
+                    const uint32_t dst = sQ + t * kTileBytes;
+                    tma_load_3d(dst, &qmap, bars.q_full(), 0, h, row, pol_q);
+                    tma_load_3d(dst + kHalfBytes, &qmap, bars.q_full(), 64, h, row, pol_q);
+                }
+                const int nkv = work.n_kv(b, 1);
+                for (int j = 0; j < nkv && ok; ++j) {
+                    for (int which = 0; which < 2; ++which, ++kv) {
+                        const int s = kv % kStages;
+                        if (kv >= kStages &&
+                            !(ok = lone_wait(bars.kv_empty(s), ((kv / kStages) & 1) ^ 1, err,
+                                             kErrWaitEmpty, abort)))
+                            break;
+                        const CUtensorMap *m = which ? &vmap : &kmap;
+                        const uint32_t dst = sRing + s * kTileBytes;
+                        mbar_arrive_expect_tx(bars.kv_full(s), kTileBytes);
+                        tma_load_3d(dst, m, bars.kv_full(s), 0, g, j * kBN, pol_kv);
+                        tma_load_3d(dst + kHalfBytes, m, bars.kv_full(s), 64, g, j * kBN,
+                                    pol_kv);
+                    }
+                }
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int kv = 0;
+            int p_cnt[kTiles] = {0, 0};
+            bool ok = true;
+            auto wait_kv = [&](int i) {
+                return lone_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err,
+                                 kErrWaitFull, abort);
+            };
+            auto issue_s = [&](int t, uint32_t ktile) {
+                const uint32_t d = tmem + kBN * t;
+                const uint32_t qtile = sQ + t * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    umma_ss(d, kmajor_desc(qtile, kk), kmajor_desc(ktile, kk), kIdescS,
+                            kk > 0);
+                umma_commit(bars.s_full(t));
+            };
+            auto issue_pv = [&](int t, uint32_t vtile, bool first) {
+                const uint32_t d = tmem + 2 * kBN + kD * t;
+                const uint32_t p = tmem + kBN * t;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    umma_ts(d, p + kk * 8, vdesc(vtile, kk), kIdescO, (!first || kk > 0));
+                umma_commit(bars.o_full(t));
+            };
+            for (int r = 0, n = 0; ok; ++r, ++n) {
+                const int idx = work.item(r, cta, G);
+                if (idx >= work.n_items) break;
+                int b, h;
+                work.coords(idx, b, h);
+                const int nA = work.n_kv(b, 0), nB = work.n_kv(b, 1);
+                if (!(ok = lone_wait(bars.q_full(), n & 1, err, kErrWaitFull, abort))) break;
+                tc_fence_after();
+                // K_0 -> S_A(0), S_B(0)
+                int kslot = kv % kStages;
+                if (!(ok = wait_kv(kv))) break;
+                tc_fence_after();
+                issue_s(0, sRing + kslot * kTileBytes);
+                issue_s(1, sRing + kslot * kTileBytes);
+                umma_commit(bars.kv_empty(kslot));
+                ++kv;
+                if (nB == 1) umma_commit(bars.q_empty());
+                for (int j = 0; j < nB && ok; ++j) {
+                    const int vslot = kv % kStages;
+                    if (!(ok = wait_kv(kv))) break;
+                    ++kv;  // kv now indexes K_{j+1}
+                    const bool next = j + 1 < nB;
+                    kslot = kv % kStages;
+                    bool k_ready = false;
+                    if (j < nA) {
+                        if (!(ok = lone_wait(bars.p_full(0), p_cnt[0] & 1, err,
+                                             kErrWaitSoftmax, abort)))
+                            break;
+                        ++p_cnt[0];
+                        tc_fence_after();
+                        issue_pv(0, sRing + vslot * kTileBytes, j == 0);
+                        if (j + 1 < nA) {
+                            if (!(ok = wait_kv(kv))) break;
+                            k_ready = true;
+                            tc_fence_after();
+                            issue_s(0, sRing + kslot * kTileBytes);
+                        }
+                    }
+                    if (!(ok = lone_wait(bars.p_full(1), p_cnt[1] & 1, err, kErrWaitSoftmax,
+                                         abort)))
+                        break;
+                    ++p_cnt[1];
+                    tc_fence_after();
+                    issue_pv(1, sRing + vslot * kTileBytes, j == 0);
+                    umma_commit(bars.kv_empty(vslot));
+                    if (next) {
+                        if (!k_ready && !(ok = wait_kv(kv))) break;
+                        tc_fence_after();
+                        issue_s(1, sRing + kslot * kTileBytes);
+                        umma_commit(bars.kv_empty(kslot));
+                        ++kv;
+                        if (j + 2 == nB) umma_commit(bars.q_empty());
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------ softmax
+        const int t = warp >> 2;             // 0 = tile A, 1 = tile B
+        const int r = (warp & 3) * 32 + lane; // row inside the tile = TMEM lane
+        const uint32_t lane_field = uint32_t((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + lane_field + kBN * t;
+        const uint32_t o_tm = tmem + lane_field + 2 * kBN + kD * t;
+        int s_cnt = 0, o_cnt = 0;
+        bool ok = true;
+        for (int rr = 0; ok; ++rr) {
+            const int idx = work.item(rr, cta, G);
+            if (idx >= work.n_items) break;
+            int b, h;
+            work.coords(idx, b, h);
+            const int qt = 2 * b + t;
+            const int n = work.n_kv(b, t);
+            const int row = qt * kBM + r;
+            float m_run = -INFINITY, l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                if (!(ok = warp_wait(bars.s_full(t), s_cnt & 1, err, kErrWaitMma, abort)))
+                    break;
+                ++s_cnt;
+                tc_fence_after();
+                uint32_t sv[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c)
+                    tmem_ld32(s_tm + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+                tmem_wait_ld();
+                // keys kbase + c with c <= lim are visible to this row
+                const int kbase = j * kBN;
+                int lim = S - 1 - kbase;
+                if (causal && row - kbase < lim) lim = row - kbase;
+                float mx = -INFINITY;
+                if (lim >= kBN - 1) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+                        mx = fmaxf(mx, __uint_as_float(sv[c]));
+                    }
+                }
+                const float m_new = fmaxf(m_run, mx * kScaleLog2);
+                float alpha = 1.f;
+                bool resc = false;
+                if (j == 0) {
+                    m_run = m_new;
+                } else if (m_new > m_run + kRescaleLog2) {
+                    alpha = ex2(m_run - m_new);
+                    m_run = m_new;
+                    l *= alpha;
+                    resc = true;
+                }
+                const float neg_m = -m_run;
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN; c += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[c]), kScaleLog2, neg_m));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), kScaleLog2, neg_m));
+                    sum += p0 + p1;
+                    sv[c >> 1] = pack_bf16(p0, p1);
+                }
+                l += sum;
+                tmem_st32(s_tm, *reinterpret_cast<uint32_t(*)[32]>(sv));
+                tmem_st32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+                tmem_wait_st();
+                if (j > 0) {
+                    // O of the previous KV tile must be complete before it is
+                    // rescaled (and before P_j is consumed, which keeps the
+                    // o_full phases matched one to one).
+                    if (!(ok = warp_wait(bars.o_full(t), o_cnt & 1, err, kErrWaitMma, abort)))
+                        break;
+                    ++o_cnt;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                        for (int c = 0; c < kD / 32; ++c) {
+                            uint32_t ov[32];
+                            tmem_ld32(o_tm + 32 * c, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tmem_st32(o_tm + 32 * c, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_full(t));
+            }
+            if (!ok) break;
+            // epilogue: out = O / l (bf16), rows past S are not stored
+            if (!(ok = warp_wait(bars.o_full(t), o_cnt & 1, err, kErrWaitMma, abort))) break;
+            ++o_cnt;
+            tc_fence_after();
+            const float inv = 1.f / l;
+            __nv_bfloat16 *dst = out + (size_t(row) * kHq + h) * kD;
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(o_tm + 32 * c, ov);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv,
+                                      __uint_as_float(ov[2 * e + 1]) * inv);
+                if (row < S) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+            }
+            tc_fence_before();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, void *out, int S, int causal,
+                           int num_sms, unsigned *err, cudaStream_t stream) {
+    static bool configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
+        e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int T = (S + kBM - 1) / kBM;
+    const int n_items = (T + 1) / 2 * kHq;
+    const int grid = n_items < num_sms ? n_items : num_sms;
+    prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
+        qmap, kmap, vmap, static_cast<__nv_bfloat16 *>(out), S, causal, err);
+    return cudaGetLastError();
+}
+
+}  // namespace gqa

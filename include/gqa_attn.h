@@ -1,0 +1,122 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) grouped-query attention forward
+ * library: causal prefill over a whole prompt and single-token decode against
+ * a KV cache.
+ *
+ * The operation (chowfi/kernels README, "Result" section and the settings
+ * line under its table): the attention step of a Llama-3-8B-size model,
+ * forward only, bf16, batch 1, 32 query heads sharing 8 KV heads, head size
+ * 128.  For query head h the KV head is g = h / 4 (4 query heads per group):
+ *
+ *     out[i,h,:] = sum_{j in J(i)} softmax_j( q[i,h,:] . k[j,g,:] / sqrt(128) ) v[j,g,:]
+ *
+ * Prefill: J(i) = {0..i} when causal ("Skip the masked half in prefill":
+ * causal attention ignores future tokens), {0..S-1} otherwise.
+ * Decode: one new query against every one of the L cached positions.
+ * Products and sums accumulate in fp32; the output is rounded to bf16 (RNE).
+ *
+ * Conventions shared by every call:
+ *  - Geometry is fixed: batch 1, 32 query heads, 8 KV heads, head dim 128.
+ *  - Tensors are bf16, contiguous, sequence-major (BSHD):
+ *      prefill  q, out [1][S][32][128]   k, v [1][S][8][128]
+ *      decode   q, out [1][1][32][128]   kcache, vcache [1][L][8][128]
+ *  - Every pointer is a DEVICE pointer on the current CUDA device, owned by
+ *    the caller, 16-byte aligned; inputs are only read, out is only written.
+ *    The library keeps no reference to them after the call returns.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream): the
+ *    result is valid once the stream reaches that point.  No call
+ *    synchronises the host, except where noted.
+ *  - Errors are status codes; no call throws.  A validation error launches
+ *    nothing and leaves `out` untouched.
+ *  - The current device must be a compute-capability 10.3 GPU (GB300).
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_ATTN_NUM_Q_HEADS 32
+#define GQA_ATTN_NUM_KV_HEADS 8
+#define GQA_ATTN_HEAD_DIM 128
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_NULL = 1,      /* a required pointer is NULL                      */
+    GQA_ERR_ALIGN = 2,     /* a pointer is not 16-byte aligned                */
+    GQA_ERR_SHAPE = 3,     /* S or L < 1, or too large for 32-bit indexing    */
+    GQA_ERR_DEVICE = 4,    /* current device is not compute capability 10.3   */
+    GQA_ERR_WORKSPACE = 5, /* caller workspace NULL, misaligned or too small  */
+    GQA_ERR_TIMEOUT = 6,   /* a bounded device-side wait ran out (see below)  */
+    GQA_ERR_CUDA = 7,      /* a CUDA runtime or driver call failed            */
+    GQA_ERR_POINTER = 8    /* a pointer is not device memory of this device   */
+} gqa_status;
+
+/*
+ * Causal (or, with causal = 0, bidirectional) prefill attention.
+ * q, out: [1][S][32][128] bf16; k, v: [1][S][8][128] bf16; 1 <= S <= 2^20.
+ * Persistent tcgen05/TMA kernel; fully masked causal tiles are skipped.
+ * Needs no workspace.  Returns GQA_OK once the kernel is enqueued.
+ */
+gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v,
+                            void *out, int S, int causal, cudaStream_t stream);
+
+/*
+ * Decode: one query token against a KV cache of length L (every cached
+ * position is attended).  q, out: [1][1][32][128] bf16; kcache, vcache:
+ * [1][L][8][128] bf16; 1 <= L <= 2^26.
+ * The KV length is split into chunks processed in parallel (each chunk reads
+ * its K/V once for all 4 query heads of a group), and a second kernel merges
+ * the chunk results with a log-sum-exp combine.  The per-chunk partial
+ * results live in a library-owned workspace allocated per device on the
+ * first call (cudaMalloc; not inside stream capture) and reused afterwards:
+ * calls on different streams of one device must not overlap in time.
+ */
+gqa_status gqa_attn_decode(const void *q, const void *kcache,
+                           const void *vcache, void *out, int L,
+                           cudaStream_t stream);
+
+/* Bytes of device workspace gqa_attn_decode_ws needs for length L (0 if L
+ * is out of range). */
+size_t gqa_attn_decode_workspace_bytes(int L);
+
+/*
+ * gqa_attn_decode with a caller-owned device workspace of at least
+ * gqa_attn_decode_workspace_bytes(L) bytes, 16-byte aligned.  Allocates
+ * nothing, so it may be captured in a CUDA graph.  The workspace must not be
+ * used by anything else until the call has completed on `stream`.
+ */
+gqa_status gqa_attn_decode_ws(const void *q, const void *kcache,
+                              const void *vcache, void *out, int L,
+                              void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
+/* Number of KV chunks (splits) the decode uses for length L on the current
+ * device; 0 if L is out of range.  Exposed for tests and the bench. */
+int gqa_attn_decode_num_splits(int L);
+
+/* Number of CUDA kernel launches one call makes (prefill: 1; decode: 2). */
+int gqa_attn_launches_per_call(int is_decode);
+
+/*
+ * Device-side error word of the current device.  Every device-side wait in
+ * the kernels is bounded (about a second); on expiry the kernel sets a bit
+ * here, abandons its work and exits cleanly instead of hanging.  This call
+ * synchronises the device, writes the word to *flags (0 = no error) and,
+ * if clear != 0, resets it.  Returns GQA_ERR_TIMEOUT if the word is
+ * non-zero, GQA_OK otherwise.
+ */
+gqa_status gqa_attn_device_error(unsigned int *flags, int clear);
+
+/* Static description of a status code. */
+const char *gqa_attn_status_string(gqa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

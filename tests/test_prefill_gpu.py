@@ -1,0 +1,80 @@
+"""Prefill (tcgen05 / TMEM / TMA kernel) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_flash_attention_causal_gb300 as gqa
+import oracle
+from gqa_flash_attention_causal_gb300.inputs import prefill_inputs
+from tests.parity import assert_close, poisoned, sample_rows, tolerance_scale
+
+pytestmark = pytest.mark.gpu
+
+# full comparisons: the 512 config, sizes around the 128-row tile and the
+# 256-row work item, ragged tails, and the degenerate S=1
+FULL = [1, 2, 3, 17, 127, 128, 129, 255, 256, 257, 300, 512, 1000]
+# sampled rows at the pages' prefill sizes (2K..32K)
+SAMPLED = [2048, 4096, 8192, 16384, 32768]
+
+
+def run(S, causal=True, stress=False):
+    q, k, v = prefill_inputs(S, stress=stress)
+    out = poisoned((1, S, 32, 128))
+    gqa.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, out=out)
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    return (q, k, v), out
+
+
+@pytest.mark.parametrize("S", FULL)
+def test_prefill_causal_full(S):
+    (q, k, v), out = run(S)
+    assert_close(out, oracle.prefill(q, k, v, causal=True)[None], what=f"causal S={S}")
+
+
+@pytest.mark.parametrize("S", [1, 129, 512, 700])
+def test_prefill_noncausal_full(S):
+    (q, k, v), out = run(S, causal=False)
+    assert_close(out, oracle.prefill(q, k, v, causal=False)[None], what=f"full S={S}")
+
+
+@pytest.mark.parametrize("S", SAMPLED)
+def test_prefill_causal_sampled(S):
+    (q, k, v), out = run(S)
+    rows = sample_rows(S)
+    want = oracle.prefill_rows(q, k, v, rows, causal=True)
+    assert_close(out[0, rows], want, what=f"causal S={S} sampled")
+    assert bool(torch.isfinite(out.float()).all()), "unwritten output rows"
+
+
+def test_prefill_stress_s4096():
+    (q, k, v), out = run(4096, stress=True)
+    rows = sample_rows(4096, n_random=64)
+    want = oracle.prefill_rows(q, k, v, rows, causal=True)
+    assert_close(out[0, rows], want, scale=tolerance_scale(v, True), what="stress")
+
+
+def test_causal_row0_is_v0_exactly():
+    (q, k, v), out = run(1000, stress=True)
+    want = v[0, 0].repeat_interleave(4, dim=0)
+    assert torch.equal(out[0, 0].cpu(), want)
+
+
+def test_prefill_gqa_packing_identical_heads():
+    S = 640
+    q, k, v = prefill_inputs(S)
+    q = q.view(1, S, 8, 4, 128)[:, :, :, :1].expand(1, S, 8, 4, 128).reshape(1, S, 32, 128)
+    out = gqa.prefill(q.contiguous().cuda(), k.cuda(), v.cuda()).view(S, 8, 4, 128)
+    torch.cuda.synchronize()
+    for j in range(1, 4):
+        assert torch.equal(out[:, :, 0], out[:, :, j])
+
+
+def test_prefill_deterministic():
+    S = 3000
+    q, k, v = prefill_inputs(S)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    a = gqa.prefill(dq, dk, dv)
+    b = gqa.prefill(dq, dk, dv)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
