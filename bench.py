@@ -162,41 +162,54 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- oracle
-def oracle_sample(seconds: float = 12.0):
-    """Time the fp64 CPU oracle on a bounded sample of the step: every query
-    row of the S=32768 prefill costs 4*H*D*(i+1) flops; rows are drawn evenly
-    over the sequence until about `seconds` of work, plus one full decode at
-    L=65536.  Returns (TFLOP/s, cores, description)."""
-    import numpy as np
-    import oracle
-    from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
+class OracleSample:
+    """Times the fp64 CPU oracle on a bounded sample of the step.
 
-    q, k, v = prefill_inputs(S_PREFILL)
-    dq, kc, vc = decode_inputs(L_DECODE)
-    cores = oracle.max_threads()
+    Every query row i of the S=32768 causal prefill costs 4*H*D*(i+1) flops;
+    rows are taken evenly over the sequence until about `seconds` of work,
+    and the decode at L=65536 is computed in full.  The rate is those flops
+    over the wall time, in TFLOP/s (the GPU metric's unit)."""
 
+    def __init__(self):
+        import oracle
+        from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
+        self.oracle = oracle
+        self.q, self.k, self.v = prefill_inputs(S_PREFILL)
+        self.dq, self.kc, self.vc = decode_inputs(L_DECODE)
+        self.cores = oracle.max_threads()
+        self.rate = None
+
+    @staticmethod
     def row_flops(rows):
-        return sum(4.0 * HQ * D * (r + 1) for r in rows)
+        return sum(4.0 * HQ * D * (int(r) + 1) for r in rows)
 
-    # calibrate on a few rows, then size the sample
-    probe = list(np.linspace(0, S_PREFILL - 1, 2 * cores).astype(int))
-    t0 = time.perf_counter()
-    oracle.prefill_rows(q, k, v, probe, causal=True)
-    t_probe = time.perf_counter() - t0
-    rate = row_flops(probe) / max(t_probe, 1e-6)
-    n_rows = int(min(S_PREFILL, max(2 * cores, seconds * rate / (4.0 * HQ * D * S_PREFILL / 2))))
-    rows = list(np.linspace(0, S_PREFILL - 1, n_rows).astype(int))
-    t0 = time.perf_counter()
-    oracle.prefill_rows(q, k, v, rows, causal=True)
-    t_pre = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle.decode(dq, kc, vc)
-    t_dec = time.perf_counter() - t0
-    flops = row_flops(rows) + decode_flops(L_DECODE)
-    desc = (f"{n_rows} of {S_PREFILL} causal prefill query rows (all 32 heads, evenly spaced) "
-            f"+ one full decode at L={L_DECODE}; fp64 C oracle, OpenMP over (row, head); "
-            f"prefill {t_pre:.2f} s, decode {t_dec:.2f} s")
-    return flops / (t_pre + t_dec) / 1e12, cores, desc, t_pre + t_dec
+    def _rows(self, n):
+        import numpy as np
+        return [int(x) for x in np.linspace(0, S_PREFILL - 1, n).astype(int)]
+
+    def calibrate(self):
+        rows = self._rows(2 * self.cores)
+        t0 = time.perf_counter()
+        self.oracle.prefill_rows(self.q, self.k, self.v, rows, causal=True)
+        self.rate = self.row_flops(rows) / max(time.perf_counter() - t0, 1e-6)
+
+    def run(self, seconds: float):
+        if self.rate is None:
+            self.calibrate()
+        t0 = time.perf_counter()
+        self.oracle.decode(self.dq, self.kc, self.vc)
+        t_dec = time.perf_counter() - t0
+        mean_row = 4.0 * HQ * D * S_PREFILL / 2
+        n = int(min(S_PREFILL, max(self.cores, (seconds - t_dec) * self.rate / mean_row)))
+        rows = self._rows(n)
+        t0 = time.perf_counter()
+        self.oracle.prefill_rows(self.q, self.k, self.v, rows, causal=True)
+        t_pre = time.perf_counter() - t0
+        flops = self.row_flops(rows) + decode_flops(L_DECODE)
+        desc = (f"{n} of {S_PREFILL} causal prefill query rows (all 32 heads, evenly spaced) "
+                f"+ one full decode at L={L_DECODE}; fp64 C oracle, OpenMP over (row, head); "
+                f"prefill {t_pre:.2f} s, decode {t_dec:.2f} s")
+        return flops / (t_pre + t_dec) / 1e12, desc, t_pre + t_dec
 
 
 # ----------------------------------------------------------------- distributed
@@ -229,32 +242,31 @@ def barrier(world: int):
 
 
 # ----------------------------------------------------------------- arms
-def run_reference(args, world, rank):
-    if rank != 0:
-        return None
-    samples = []
+def run_reference(args, n_world):
+    """The oracle as it stands, on the host cores: W warm-up and K timed
+    steps, each a bounded sample of the step sized so the whole run takes
+    about --ref-total seconds."""
+    sample = OracleSample()
+    secs = min(args.ref_seconds, max(1.0, args.ref_total / (args.steps + args.warmup)))
     for _ in range(args.warmup):
-        pass  # the oracle has no warm state worth burning in beyond the first call
-    per_step = []
-    desc = ""
-    cores = 0
+        sample.run(secs)
+    rates, times, desc = [], [], ""
     for _ in range(args.steps):
-        tf, cores, desc, secs = oracle_sample(seconds=args.ref_seconds)
-        samples.append(tf)
-        per_step.append(secs)
-    value = statistics.median(samples)
-    line = {
+        tf, desc, t = sample.run(secs)
+        rates.append(tf)
+        times.append(t)
+    value = statistics.median(rates)
+    return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * statistics.median(per_step), "higher_is_better": True,
+        "n_gpus": n_world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": desc},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": sample.cores,
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    return line
 
 
 def run_ours(args, world, rank, local):
@@ -355,8 +367,10 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        tf, cores, desc, _ = oracle_sample(seconds=args.ref_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        sample = OracleSample()
+        tf, desc, _ = sample.run(args.ref_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
+               "sample": desc}
 
     clk = clocks.summary()
     traffic = profiled_traffic("prefill")
@@ -422,26 +436,28 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-seconds", type=float, default=12.0,
-                    help="CPU seconds of oracle work per reference step / baseline")
+                    help="CPU seconds of oracle work for the baseline (at most, per step)")
+    ap.add_argument("--ref-total", type=float, default=150.0,
+                    help="CPU seconds the whole reference arm should take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     world, rank, local = dist_env()
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; other ranks exit without work
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world)))
+        return 0
     if world > 1:
+        import torch
         import torch.distributed as dist
-        if args.impl == "reference":
-            if rank != 0:
-                return 0
-            world = 1
-        else:
-            import torch
-            torch.cuda.set_device(local)
-            dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
     try:
-        line = run_reference(args, world, rank) if args.impl == "reference" else \
-            run_ours(args, world, rank, local)
+        line = run_ours(args, world, rank, local)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -1,0 +1,56 @@
+"""Host-side multi-rank logic of bench.py on CPU (gloo, world size 2):
+whole-job time is the max over ranks and work is the sum over ranks."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, units = bench.aggregate(10.0 + 5.0 * rank, 100.0 * (rank + 1), world)
+        q.put((rank, ms, units))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_max_time_sum_work():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(world))
+    for rank, ms, units in got:
+        assert ms == 15.0 and units == 300.0
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_warmup_minimum():
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
