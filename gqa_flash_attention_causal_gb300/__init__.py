@@ -32,6 +32,7 @@ SIGNATURES = {
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_workspace_bytes": (_S, [_I]),
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
+    "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_num_splits": (_I, [_I]),
     "gqa_attn_launches_per_call": (_I, [_I]),
     "gqa_attn_device_error": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
@@ -136,6 +137,22 @@ def decode(q, kcache, vcache, out=None, workspace=None, stream=None):
         _check("gqa_attn_decode_ws", lib().gqa_attn_decode_ws(
             q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(), L,
             workspace.data_ptr(), nbytes, s))
+    return out
+
+
+def decode_noalloc(q, kcache, vcache, out, stream=None):
+    """Decode through the entry point that allocates nothing (its partial
+    results use the library's fixed 1 MiB scratch; calls on one device must
+    not overlap in time).  ``out`` must be given: this call allocates no
+    tensor either."""
+    L = kcache.shape[1]
+    _expect(q, (1, 1, HQ, HEAD_DIM), "q")
+    _expect(kcache, (1, L, HKV, HEAD_DIM), "kcache")
+    _expect(vcache, (1, L, HKV, HEAD_DIM), "vcache")
+    _expect(out, (1, 1, HQ, HEAD_DIM), "out")
+    _check("gqa_attn_decode_noalloc", lib().gqa_attn_decode_noalloc(
+        q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(), L,
+        _stream(stream)))
     return out
 
 

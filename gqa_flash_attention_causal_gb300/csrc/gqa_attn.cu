@@ -13,6 +13,14 @@ using gqa::kHkv;
 using gqa::kHq;
 using gqa::kMaxDevices;
 
+// Fixed scratch of gqa_attn_decode_noalloc: the decode's per-chunk partial
+// results live here instead of in allocated memory.  1 MiB holds the
+// partials of up to 63 chunks (a 152-SM GB300 uses at most 38).  Every GPU
+// that loads this library holds one copy until the process exits, and all
+// calls on a device share it.
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 // Per-device word the kernels OR their error bits into (bounded waits that
@@ -29,6 +37,7 @@ struct DeviceState {
     unsigned *err = nullptr;       // device address of g_device_error
     void *workspace = nullptr;     // decode partials (library-owned)
     size_t workspace_bytes = 0;
+    void *scratch = nullptr;       // device address of g_decode_scratch
 };
 
 std::mutex g_mu;
@@ -143,6 +152,23 @@ gqa_status decode_args(const void *q, const void *kc, const void *vc, void *out,
     return GQA_OK;
 }
 
+// Device address of this device's copy of g_decode_scratch.  In host code the
+// array's name only stands for the symbol, so the address is looked up once
+// per device, with that device current, and cached.
+gqa_status decode_scratch(DeviceState *dev, void **out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!dev->scratch) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return GQA_ERR_CUDA;
+        }
+        dev->scratch = p;
+    }
+    *out = dev->scratch;
+    return GQA_OK;
+}
+
 gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, int L,
                       const gqa::DecodePlan &plan, void *ws, unsigned *err,
                       cudaStream_t stream) {
@@ -233,6 +259,19 @@ gqa_status gqa_attn_decode(const void *q, const void *kcache, const void *vcache
         }
     }
     return run_decode(q, kcache, vcache, out, L, plan, dev->workspace, dev->err, stream);
+}
+
+gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
+                                   void *out, int L, cudaStream_t stream) {
+    DeviceState *dev = nullptr;
+    gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
+    if (st != GQA_OK) return st;
+    const gqa::DecodePlan plan = gqa::decode_plan(L, dev->num_sms);
+    if (gqa::decode_workspace_bytes(plan) > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    st = decode_scratch(dev, &scratch);
+    if (st != GQA_OK) return st;
+    return run_decode(q, kcache, vcache, out, L, plan, scratch, dev->err, stream);
 }
 
 int gqa_attn_launches_per_call(int is_decode) { return is_decode ? 2 : 1; }

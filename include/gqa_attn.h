@@ -95,6 +95,33 @@ gqa_status gqa_attn_decode_ws(const void *q, const void *kcache,
                               void *workspace, size_t workspace_bytes,
                               cudaStream_t stream);
 
+/*
+ * gqa_attn_decode for callers that cannot allocate device memory: it calls
+ * no cudaMalloc, cudaFree or other allocating routine.  (The pages have no
+ * counterpart; this is a deployment need.)  Such callers include serving
+ * processes whose device memory is entirely handed to their own pool (for
+ * instance a KV-cache pool sized to all free HBM, where one more cudaMalloc
+ * fails or fragments the pool) and processes running under a fixed device
+ * memory budget that forbids allocations after start-up.
+ *
+ * Arguments, layouts and results are those of gqa_attn_decode; the caller
+ * still passes the inputs and the output.  The per-chunk partial results go
+ * to a fixed 1 MiB scratch array compiled into the library (every GPU that
+ * loads the library holds one copy until the process exits).
+ *  - The first call on a device looks up that device's copy of the array
+ *    (once per device); make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    partials: calls that overlap in time on the GPU (e.g. on two streams)
+ *    race and give wrong results.  Nothing in it needs to start at zero:
+ *    each call writes every partial it reads.
+ *  - If length L would need more scratch than 1 MiB on this device (more
+ *    than 63 chunks; a 152-SM GB300 uses at most 38), the call returns
+ *    GQA_ERR_WORKSPACE and launches nothing.
+ */
+gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache,
+                                   const void *vcache, void *out, int L,
+                                   cudaStream_t stream);
+
 /* Number of KV chunks (splits) the decode uses for length L on the current
  * device; 0 if L is out of range.  Exposed for tests and the bench. */
 int gqa_attn_decode_num_splits(int L);
