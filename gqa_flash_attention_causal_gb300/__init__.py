@@ -37,6 +37,7 @@ SIGNATURES = {
     "gqa_attn_launches_per_call": (_I, [_I]),
     "gqa_attn_device_error": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
     "gqa_attn_status_string": (ctypes.c_char_p, [_I]),
+    "gqa_attn_last_error_string": (ctypes.c_char_p, []),
 }
 
 _lib = None
@@ -48,6 +49,10 @@ class GqaError(RuntimeError):
     def __init__(self, fn: str, code: int):
         self.code = code
         msg = lib().gqa_attn_status_string(code).decode()
+        if code == 7:
+            detail = lib().gqa_attn_last_error_string().decode()
+            if detail:
+                msg += f"; {detail}"
         super().__init__(f"{fn}: {STATUS.get(code, code)} ({msg})")
 
 

@@ -242,26 +242,78 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // Merge the chunk results of every query head: with per-chunk normalised
-// outputs O_c and log2-sum-exp values lse_c,
+// outputs O_c and base-2 log-sum-exp values lse_c,
 //   out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M),  M = max_c lse_c.
-__global__ void __launch_bounds__(kD)
+// One CTA per query head; warp w merges chunks w, w+8, ... (lane = 4 dims)
+// with a running maximum, then warp 0 merges the 8 warps' states.
+constexpr int kCmbWarps = 8;
+constexpr int kCmbUnroll = 4;
+
+__global__ void __launch_bounds__(kCmbWarps * 32)
 decode_combine_kernel(const float *__restrict__ part_o,
                       const float *__restrict__ part_lse, int n_split,
                       __nv_bfloat16 *__restrict__ out) {
     // Launched as a programmatic dependent of the split kernel: wait until
     // its results are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int h = blockIdx.x, d = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_lse[s * kHq + h]);
-    float num = 0.f, den = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < n_split; ++s) {
-        const float w = ex2(part_lse[s * kHq + h] - M);
-        den += w;
-        num += w * part_o[(size_t(s) * kHq + h) * kD + d];
+    __shared__ float s_m[kCmbWarps], s_den[kCmbWarps];
+    __shared__ float4 s_acc[kCmbWarps][32];
+    const int h = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d0 = lane * 4;
+    float m = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = w; s0 < n_split; s0 += kCmbWarps * kCmbUnroll) {
+        float l[kCmbUnroll];
+        float4 o[kCmbUnroll];
+#pragma unroll
+        for (int u = 0; u < kCmbUnroll; ++u) {  // issue every load first
+            const int s = s0 + u * kCmbWarps;
+            if (s < n_split) {
+                l[u] = __ldcg(part_lse + s * kHq + h);
+                o[u] = __ldcg(reinterpret_cast<const float4 *>(
+                    part_o + (size_t(s) * kHq + h) * kD + d0));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCmbUnroll; ++u) {
+            if (s0 + u * kCmbWarps >= n_split) break;
+            if (l[u] > m) {
+                const float sc = ex2(m - l[u]);  // 0 while m is -inf
+                den *= sc;
+                acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+                m = l[u];
+            }
+            const float wt = ex2(l[u] - m);
+            den += wt;
+            acc.x += wt * o[u].x; acc.y += wt * o[u].y;
+            acc.z += wt * o[u].z; acc.w += wt * o[u].w;
+        }
     }
-    out[h * kD + d] = __float2bfloat16_rn(num / den);
+    if (lane == 0) {
+        s_m[w] = m;
+        s_den[w] = den;
+    }
+    s_acc[w][lane] = acc;
+    __syncthreads();
+    if (w != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kCmbWarps; ++i) M = fmaxf(M, s_m[i]);
+    float tden = 0.f;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kCmbWarps; ++i) {
+        if (s_m[i] == -INFINITY) continue;  // a warp with no chunk
+        const float f = ex2(s_m[i] - M);
+        tden += f * s_den[i];
+        const float4 a = s_acc[i][lane];
+        t.x += f * a.x; t.y += f * a.y; t.z += f * a.z; t.w += f * a.w;
+    }
+    const float inv = 1.f / tden;
+    uint2 pk;
+    pk.x = pack_bf16(t.x * inv, t.y * inv);
+    pk.y = pack_bf16(t.z * inv, t.w * inv);
+    *reinterpret_cast<uint2 *>(out + h * kD + d0) = pk;
 }
 
 }  // namespace
@@ -309,7 +361,7 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kHq);
-    cfg.blockDim = dim3(kD);
+    cfg.blockDim = dim3(kCmbWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -2,6 +2,7 @@
 // argument validation, per-device state (SM count, error word, decode
 // workspace), TMA tensor-map encoding and kernel dispatch.
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -43,6 +44,14 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+// Text of the last failing CUDA call on this host thread.
+thread_local char t_last_error[160] = "";
+
+void note_error(const char *what, cudaError_t e) {
+    snprintf(t_last_error, sizeof t_last_error, "%s: %s (%d)", what, cudaGetErrorString(e),
+             int(e));
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave,
@@ -66,7 +75,9 @@ EncodeTiledFn encode_fn() {
 // Current device's state, probing it on first use.
 gqa_status current_device(DeviceState **out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess) {
+        note_error("cudaGetDevice", ge);
         cudaGetLastError();
         return GQA_ERR_CUDA;
     }
@@ -127,11 +138,17 @@ gqa_status encode_bshd(CUtensorMap *m, const void *base, int rows, int heads, in
                     strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        snprintf(t_last_error, sizeof t_last_error, "cuTensorMapEncodeTiled: CUresult %d",
+                 int(r));
+        return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
 }
 
 gqa_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return GQA_OK;
+    note_error("kernel launch", e);
     cudaGetLastError();
     return GQA_ERR_CUDA;
 }
@@ -297,6 +314,8 @@ gqa_status gqa_attn_device_error(unsigned int *flags, int clear) {
     *flags = word;
     return word ? GQA_ERR_TIMEOUT : GQA_OK;
 }
+
+const char *gqa_attn_last_error_string(void) { return t_last_error; }
 
 const char *gqa_attn_status_string(gqa_status s) {
     switch (s) {

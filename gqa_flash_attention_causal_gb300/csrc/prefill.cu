@@ -343,17 +343,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 const int kbase = j * kBN;
                 int lim = S - 1 - kbase;
                 if (causal && row - kbase < lim) lim = row - kbase;
-                float mx = -INFINITY;
-                if (lim >= kBN - 1) {
+                if (lim < kBN - 1) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
+                    for (int c = 0; c < kBN; ++c)
                         if (c > lim) sv[c] = __float_as_uint(-INFINITY);
-                        mx = fmaxf(mx, __uint_as_float(sv[c]));
-                    }
                 }
+                // row max: 8 independent chains of 3-input max, then a tree
+                float mx8[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    mx8[c] = fmaxf(__uint_as_float(sv[c]), __uint_as_float(sv[c + 8]));
+#pragma unroll
+                for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        mx8[e] = fmax3(mx8[e], __uint_as_float(sv[c + e]),
+                                       __uint_as_float(sv[c + 8 + e]));
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_run, mx * kScaleLog2);
                 float alpha = 1.f;
                 bool resc = false;
@@ -365,16 +372,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     l *= alpha;
                     resc = true;
                 }
-                const float neg_m = -m_run;
-                float sum = 0.f;
+                // p = 2^(s*scale*log2e - m): one packed FFMA per two scores,
+                // one MUFU ex2 per score, row sum in 4 packed accumulators
+                const float2 scale2 = make_float2(kScaleLog2, kScaleLog2);
+                const float2 neg_m2 = make_float2(-m_run, -m_run);
+                float2 sum2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sum2[e] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < kBN; c += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[c]), kScaleLog2, neg_m));
-                    const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), kScaleLog2, neg_m));
-                    sum += p0 + p1;
-                    sv[c >> 1] = pack_bf16(p0, p1);
+                    const float2 x = ffma2(make_float2(__uint_as_float(sv[c]),
+                                                       __uint_as_float(sv[c + 1])),
+                                           scale2, neg_m2);
+                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                    sum2[(c >> 1) & 3] = fadd2(sum2[(c >> 1) & 3], pp);
+                    sv[c >> 1] = pack_bf16(pp.x, pp.y);
                 }
-                l += sum;
+                const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
+                l += (s01.x + s01.y) + (s23.x + s23.y);
                 tmem_st32(s_tm, *reinterpret_cast<uint32_t(*)[32]>(sv));
                 tmem_st32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
                 tmem_wait_st();

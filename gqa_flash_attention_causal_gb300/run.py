@@ -14,7 +14,7 @@ import statistics
 
 import torch
 
-from . import decode, prefill
+from . import decode, decode_workspace_bytes, prefill
 from .inputs import decode_inputs, prefill_inputs
 
 
@@ -30,12 +30,51 @@ def _time(fn, iters):
     return statistics.median(times[1:] if len(times) > 1 else times)
 
 
+def _time_graph(fn, reps, iters):
+    """Median time of one call, from a CUDA graph of `reps` back-to-back calls
+    (removes host launch gaps)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm-up outside capture (first-call set-up)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                fn()
+    torch.cuda.current_stream().wait_stream(s)
+    times = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    return statistics.median(times[1:] if len(times) > 1 else times)
+
+
+def _host_us(fn, n=200):
+    """Host time of one call (enqueue only), microseconds."""
+    import time
+    fn()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        fn()
+    t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    return (t1 - t0) / n * 1e6
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--prefill", type=int, default=0, help="prompt length S (0 = skip)")
     ap.add_argument("--non-causal", action="store_true")
     ap.add_argument("--decode", type=int, default=0, help="KV cache length L (0 = skip)")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--graph", type=int, default=0,
+                    help="also time decode as a CUDA graph of this many back-to-back calls")
+    ap.add_argument("--host", action="store_true", help="also report host time per call")
     args = ap.parse_args(argv)
     dev = torch.device("cuda")
     if args.prefill:
@@ -52,7 +91,15 @@ def main(argv=None):
         out = torch.empty_like(q)
         ms = _time(lambda: decode(q, kc, vc, out=out), args.iters)
         nbytes = 2.0 * L * 8 * 128 * 2 + 2 * 32 * 128 * 2
-        print(f"decode L={L}: {ms * 1e3:.2f} us, {nbytes / ms / 1e6:.1f} GB/s")
+        line = f"decode L={L}: {ms * 1e3:.2f} us, {nbytes / ms / 1e6:.1f} GB/s"
+        if args.graph:
+            ws = torch.empty(decode_workspace_bytes(L), dtype=torch.uint8, device=dev)
+            gms = _time_graph(lambda: decode(q, kc, vc, out=out, workspace=ws), args.graph,
+                              max(args.iters, 3))
+            line += f"; graph {gms * 1e3:.2f} us, {nbytes / gms / 1e6:.1f} GB/s"
+        if args.host:
+            line += f"; host {_host_us(lambda: decode(q, kc, vc, out=out)):.1f} us/call"
+        print(line)
 
 
 if __name__ == "__main__":

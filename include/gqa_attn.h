@@ -139,6 +139,12 @@ int gqa_attn_launches_per_call(int is_decode);
  */
 gqa_status gqa_attn_device_error(unsigned int *flags, int clear);
 
+/* Text of the most recent failing CUDA call made by this library on the
+ * calling host thread (the reason behind a GQA_ERR_CUDA), or "" if none.
+ * The string is owned by the library and valid until the thread's next
+ * call into it. */
+const char *gqa_attn_last_error_string(void);
+
 /* Static description of a status code. */
 const char *gqa_attn_status_string(gqa_status status);
 
