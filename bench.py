@@ -74,10 +74,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {"prefill": ("prefill.cu", "ptx.cuh", "internal.h"),
+                  "decode": ("decode.cu", "ptx.cuh", "internal.h")}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the source files that define `kernel` (prefill or decode)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_flash_attention_causal_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -91,7 +96,7 @@ def profiled_traffic(kernel: str):
             rec = json.load(f)[kernel]
     except Exception:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("bytes_per_launch")
 
