@@ -38,6 +38,7 @@ SIGNATURES = {
     "gqa_attn_device_error": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
     "gqa_attn_status_string": (ctypes.c_char_p, [_I]),
     "gqa_attn_last_error_string": (ctypes.c_char_p, []),
+    "gqa_attn_selftest_wait_timeout": (_I, [ctypes.POINTER(ctypes.c_uint)]),
 }
 
 _lib = None

@@ -315,6 +315,19 @@ gqa_status gqa_attn_device_error(unsigned int *flags, int clear) {
     return word ? GQA_ERR_TIMEOUT : GQA_OK;
 }
 
+gqa_status gqa_attn_selftest_wait_timeout(unsigned int *flags) {
+    if (!flags) return GQA_ERR_NULL;
+    unsigned before = 0;
+    gqa_status st = gqa_attn_device_error(&before, 1);  // start from a clear word
+    if (st != GQA_OK && st != GQA_ERR_TIMEOUT) return st;
+    DeviceState *dev = nullptr;
+    st = current_device(&dev);
+    if (st != GQA_OK) return st;
+    st = from_cuda(gqa::launch_wait_timeout_selftest(dev->err, 0));
+    if (st != GQA_OK) return st;
+    return gqa_attn_device_error(flags, 1);
+}
+
 const char *gqa_attn_last_error_string(void) { return t_last_error; }
 
 const char *gqa_attn_status_string(gqa_status s) {

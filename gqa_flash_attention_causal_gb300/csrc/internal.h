@@ -37,4 +37,9 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, void *out, int S, int causal,
                            int num_sms, unsigned *err, cudaStream_t stream);
 
+// ------------------------------------------------------------------ self-test
+// Error bit the self-test kernel's deliberately expiring wait sets.
+constexpr unsigned kErrSelfTestBit = 1u << 31;
+cudaError_t launch_wait_timeout_selftest(unsigned *err, cudaStream_t stream);
+
 }  // namespace gqa

@@ -139,6 +139,18 @@ int gqa_attn_launches_per_call(int is_decode);
  */
 gqa_status gqa_attn_device_error(unsigned int *flags, int clear);
 
+/*
+ * Self-test of the failure path behind GQA_ERR_TIMEOUT (the pages have no
+ * counterpart).  Launches a one-CTA kernel on the legacy default stream that
+ * waits, through the same bounded wait the kernels use, on a barrier that
+ * nothing arrives at.  The wait gives up after its limit (about a second),
+ * sets bit 31 of the device error word and returns; no fault, no trap, and
+ * the context stays usable.  Synchronises the device, clears the word before
+ * and after, and stores the word the kernel left in *flags.  Returns
+ * GQA_ERR_TIMEOUT when the wait ran out as designed.
+ */
+gqa_status gqa_attn_selftest_wait_timeout(unsigned int *flags);
+
 /* Text of the most recent failing CUDA call made by this library on the
  * calling host thread (the reason behind a GQA_ERR_CUDA), or "" if none.
  * The string is owned by the library and valid until the thread's next
