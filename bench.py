@@ -292,15 +292,35 @@ def run_ours(args, world, rank, local):
     dout = torch.empty_like(d_dq)
     stream = torch.cuda.current_stream()
 
-    def step():
+    ws = torch.empty(gqa.decode_workspace_bytes(L_DECODE), dtype=torch.uint8, device=dev)
+
+    def run_prefill():
         gqa.prefill(d_q, d_k, d_v, causal=True, out=out)
-        gqa.decode(d_dq, d_kc, d_vc, out=dout)
+
+    def run_decode():
+        gqa.decode(d_dq, d_kc, d_vc, out=dout, workspace=ws)
 
     for _ in range(max(3, args.warmup)):
-        step()
+        run_prefill()
+        run_decode()
     torch.cuda.synchronize()
     if gqa.device_error() != 0:
         raise RuntimeError("device-side wait timed out during warm-up")
+
+    # Each half of the step is captured once as a CUDA graph and replayed, so
+    # the timed region holds no host launch gaps between kernels.
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_pre, stream=side):
+            run_prefill()
+        with torch.cuda.graph(g_dec, stream=side):
+            run_decode()
+    stream.wait_stream(side)
+    g_pre.replay()
+    g_dec.replay()
+    torch.cuda.synchronize()
 
     # ------------------------------------------------ timed region (device)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -311,9 +331,9 @@ def run_ours(args, world, rank, local):
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            gqa.prefill(d_q, d_k, d_v, causal=True, out=out)
+            g_pre.replay()
             ev[i][1].record(stream)
-            gqa.decode(d_dq, d_kc, d_vc, out=dout)
+            g_dec.replay()
             ev[i][2].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -399,6 +419,7 @@ def run_ours(args, world, rank, local):
             "kv_len": L_DECODE,
             "parallelism": f"replicas{world}",
             "l2": "inputs larger than L2 (prefill q 256 MiB + k,v 128 MiB; decode KV 256 MiB)",
+            "launch": "each step replays a CUDA graph of the prefill and one of the decode",
         },
         "roofline": {
             "kernel": "prefill_kernel",

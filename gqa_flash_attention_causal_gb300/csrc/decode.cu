@@ -14,8 +14,8 @@
 //  * softmax in base 2 with log2(e) folded into the score scale (item 5).
 //
 // The work is HBM-bound (4 flops per byte), so the design goal is keeping
-// enough bytes in flight: K/V tiles stream through a 3-stage TMA ring, two
-// CTAs per SM.  The 16-key x 128-dim x 4-head products go through warp-level
+// enough bytes in flight: K/V tiles stream through a 6-stage TMA ring (192 KB
+// in flight per SM), one CTA per SM.  The 16-key x 128-dim x 4-head products go through warp-level
 // bf16 MMA (m16n8k16) with fp32 accumulation: one ldmatrix + one MMA replaces
 // 256 scalar FMAs, which keeps instruction issue far below the memory time.
 #include <cuda_bf16.h>
@@ -28,12 +28,12 @@ namespace {
 
 constexpr int kWarps = 4;                        // compute warps per CTA
 constexpr int kStageKeys = 16 * kWarps;          // 64 keys per stage
-constexpr int kStages = 3;                       // TMA ring depth
+constexpr int kStages = 6;                       // TMA ring depth
 constexpr int kHalfBytes = kStageKeys * 128;     // 64 keys x 64 dims x 2 B
 constexpr int kTileBytes = 2 * kHalfBytes;       // K (or V) tile, 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;      // K + V, 32 KB
 constexpr int kThreads = (kWarps + 1) * 32;      // + one TMA producer warp
-constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSm = 1;
 constexpr int kCmbFloats = kWarps * kGroup * kD; // cross-warp merge buffer
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + size_t(kStages) * kStageBytes +
                               size_t(kCmbFloats) * 4 + 2 * kWarps * kGroup * 4 +
@@ -77,13 +77,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         fence_barrier_init();
     }
+    if (threadIdx.x == kWarps * 32) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+    }
     __syncthreads();
+    // Launched as a programmatic dependent of whatever kernel precedes it on
+    // the stream: everything above overlapped that kernel's tail; from here
+    // on its results (q, the caches) are complete and visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == kWarps) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
             const uint64_t pol = policy_evict_first();
             for (int it = 0; it < n_iter; ++it) {
                 const int s = it % kStages;
@@ -353,22 +359,27 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     float *part_o = static_cast<float *>(workspace);
     float *part_lse = part_o + size_t(plan.n_split) * kHq * kD;
 
-    decode_split_kernel<<<dim3(plan.n_split, kHkv), kThreads, kSmemBytes, stream>>>(
-        kmap, vmap, static_cast<const __nv_bfloat16 *>(q), L, plan.chunk, part_o, part_lse,
-        err);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kHq);
-    cfg.blockDim = dim3(kCmbWarps * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
+    // Both kernels are programmatic dependents of their predecessor on the
+    // stream: their launch and set-up overlap it, and each waits
+    // (griddepcontrol.wait) before reading anything the predecessor wrote.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.n_split, kHkv);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_split_kernel, kmap, vmap,
+                           static_cast<const __nv_bfloat16 *>(q), L, plan.chunk, part_o,
+                           part_lse, err);
+    if (e != cudaSuccess) return e;
+
+    cfg.gridDim = dim3(kHq);
+    cfg.blockDim = dim3(kCmbWarps * 32);
+    cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel,
                               static_cast<const float *>(part_o),
                               static_cast<const float *>(part_lse), plan.n_split,

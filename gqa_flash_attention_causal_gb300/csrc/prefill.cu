@@ -179,17 +179,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    if (warp == kWarpLoad && lane == 0) {
+        prefetch_tmap(&qmap);
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the preceding kernel on the
+    // stream: the set-up above overlapped its tail; wait for its results
+    // before reading q/k/v or writing out.  The next kernel may launch now
+    // (it waits for this grid in the same way).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&qmap);
-            prefetch_tmap(&kmap);
-            prefetch_tmap(&vmap);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
             int kv = 0;
@@ -473,9 +481,18 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
     const int T = (S + kBM - 1) / kBM;
     const int n_items = (T + 1) / 2 * kHq;
     const int grid = n_items < num_sms ? n_items : num_sms;
-    prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-        qmap, kmap, vmap, static_cast<__nv_bfloat16 *>(out), S, causal, err);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel, qmap, kmap, vmap,
+                              static_cast<__nv_bfloat16 *>(out), S, causal, err);
 }
 
 }  // namespace gqa
