@@ -454,6 +454,98 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def run_sweep(args):
+    """One JSON line per configuration of the pages' Result table (plus the
+    S=512 and stress cases): GPU time, throughput, fraction of roofline,
+    error against the fp64 oracle on sampled rows, and the oracle's own time
+    on this host (measured on the sampled rows, scaled by FLOPs)."""
+    import numpy as np
+    import torch
+    import gqa_flash_attention_causal_gb300 as gqa
+    import oracle
+    from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
+    peaks, src = load_peaks()
+    dev = torch.device("cuda")
+    gqa.lib()
+    rng = np.random.default_rng(0)
+
+    def med_time(fn, n=5):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    cases = [("prefill", S, False) for S in (512, 2048, 4096, 8192, 16384, 32768)]
+    cases += [("prefill", 4096, True)]
+    cases += [("decode", L, False) for L in (2048, 4096, 8192, 16384, 32768, 65536)]
+    cases += [("decode", 32768, True)]
+    for kind, n, stress in cases:
+        if kind == "prefill":
+            q, k, v = prefill_inputs(n, stress=stress)
+            dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+            out = torch.empty_like(dq)
+            ms = med_time(lambda: gqa.prefill(dq, dk, dv, causal=True, out=out))
+            rows = sorted({0, 1, n - 1, n // 2} | set(rng.integers(0, n, 30).tolist()))
+            t0 = time.perf_counter()
+            want = oracle.prefill_rows(q, k, v, rows, causal=True)
+            t_or = time.perf_counter() - t0
+            got = out[0, rows].double().cpu().numpy()
+            sample_flops = sum(4.0 * HQ * D * (r + 1) for r in rows)
+            oracle_ms = 1e3 * t_or * (2.0 * HQ * D * n * (n + 1)) / sample_flops
+            tput = prefill_flops(n) / (ms * 1e-3) / 1e12
+            line = {"workload": "prefill", "S": n, "stress": stress, "ms": ms, "tflops": tput,
+                    "frac_of_burst": tput / peaks["bf16_tflops"],
+                    "frac_of_sustained": tput / peaks["bf16_tflops_sustained"]}
+        else:
+            q, kc, vc = decode_inputs(n, stress=stress)
+            dq = q.to(dev)
+            l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+            copies = max(1, -(-2 * l2 // (4 * kc.numel())) + 1)
+            caches = [(kc.to(dev), vc.to(dev)) for _ in range(copies)]
+            ws = torch.empty(gqa.decode_workspace_bytes(n), dtype=torch.uint8, device=dev)
+            out = torch.empty_like(dq)
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                gqa.decode(dq, *caches[0], out=out, workspace=ws)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    for c in caches:
+                        gqa.decode(dq, *c, out=out, workspace=ws)
+            torch.cuda.current_stream().wait_stream(side)
+            ms = med_time(g.replay) / copies
+            gqa.decode(dq, *caches[0], out=out, workspace=ws)
+            t0 = time.perf_counter()
+            want = oracle.decode(q, kc, vc)
+            oracle_ms = 1e3 * (time.perf_counter() - t0)
+            got = out.double().cpu().numpy().reshape(want.shape)
+            tput = decode_bytes(n) / (ms * 1e-3) / 1e9
+            line = {"workload": "decode", "L": n, "stress": stress, "ms": ms, "gbs": tput,
+                    "frac_of_measured_hbm": tput / peaks["hbm_gbs"],
+                    "frac_of_8tbs": tput / NORTH_STAR_HBM_GBS, "cache_copies": copies}
+            del caches
+        torch.cuda.synchronize()
+        err = np.abs(got - want)
+        scale = float(v.float().abs().max()) if kind == "prefill" and stress else (
+            float(vc.float().abs().max()) if stress else 1.0)
+        line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
+                     "tolerance_scale": scale,
+                     "parity_ok": bool(err.max() <= 2e-2 * scale and err.mean() <= 2e-3 * scale),
+                     "oracle_ms_est": oracle_ms, "oracle_cores": oracle.max_threads(),
+                     "peaks": src})
+        print(json.dumps(line), flush=True)
+        if gqa.device_error() != 0:
+            raise RuntimeError("device-side wait timed out")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -466,11 +558,16 @@ def main(argv=None):
     ap.add_argument("--ref-total", type=float, default=150.0,
                     help="CPU seconds the whole reference arm should take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the step, print one line per configuration of the "
+                         "pages' Result table (time, throughput, roofline, parity)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     world, rank, local = dist_env()
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         # rank 0 alone times the oracle; other ranks exit without work
         if rank != 0:
