@@ -484,23 +484,29 @@ def run_sweep(args):
 
     cases = [("prefill", S, False) for S in (512, 2048, 4096, 8192, 16384, 32768)]
     cases += [("prefill", 4096, True)]
+    cases += [("prefill_full", S, False) for S in (4096, 16384)]
     cases += [("decode", L, False) for L in (2048, 4096, 8192, 16384, 32768, 65536)]
     cases += [("decode", 32768, True)]
     for kind, n, stress in cases:
-        if kind == "prefill":
+        if kind.startswith("prefill"):
+            causal = kind == "prefill"
             q, k, v = prefill_inputs(n, stress=stress)
             dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
             out = torch.empty_like(dq)
-            ms = med_time(lambda: gqa.prefill(dq, dk, dv, causal=True, out=out))
+            ms = med_time(lambda: gqa.prefill(dq, dk, dv, causal=causal, out=out))
             rows = sorted({0, 1, n - 1, n // 2} | set(rng.integers(0, n, 30).tolist()))
             t0 = time.perf_counter()
-            want = oracle.prefill_rows(q, k, v, rows, causal=True)
+            want = oracle.prefill_rows(q, k, v, rows, causal=causal)
             t_or = time.perf_counter() - t0
             got = out[0, rows].double().cpu().numpy()
-            sample_flops = sum(4.0 * HQ * D * (r + 1) for r in rows)
-            oracle_ms = 1e3 * t_or * (2.0 * HQ * D * n * (n + 1)) / sample_flops
-            tput = prefill_flops(n) / (ms * 1e-3) / 1e12
-            line = {"workload": "prefill", "S": n, "stress": stress, "ms": ms, "tflops": tput,
+            if causal:
+                sample_flops = sum(4.0 * HQ * D * (r + 1) for r in rows)
+                oracle_ms = 1e3 * t_or * (2.0 * HQ * D * n * (n + 1)) / sample_flops
+                tput = prefill_flops(n) / (ms * 1e-3) / 1e12
+            else:
+                oracle_ms = 1e3 * t_or * n / len(rows)
+                tput = 2.0 * prefill_flops(n) / (ms * 1e-3) / 1e12  # 4*S^2*H*D
+            line = {"workload": kind, "S": n, "stress": stress, "ms": ms, "tflops": tput,
                     "frac_of_burst": tput / peaks["bf16_tflops"],
                     "frac_of_sustained": tput / peaks["bf16_tflops_sustained"]}
         else:
@@ -533,7 +539,7 @@ def run_sweep(args):
             del caches
         torch.cuda.synchronize()
         err = np.abs(got - want)
-        scale = float(v.float().abs().max()) if kind == "prefill" and stress else (
+        scale = float(v.float().abs().max()) if kind.startswith("prefill") and stress else (
             float(vc.float().abs().max()) if stress else 1.0)
         line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
                      "tolerance_scale": scale,

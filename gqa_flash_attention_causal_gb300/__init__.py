@@ -29,6 +29,8 @@ STATUS = {
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _P]),
+    "gqa_attn_prefill_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "gqa_attn_decode_lse": (_I, [_P, _P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_workspace_bytes": (_S, [_I]),
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
@@ -99,11 +101,12 @@ def _expect(t, shape, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def prefill(q, k, v, causal: bool = True, out=None, stream=None):
+def prefill(q, k, v, causal: bool = True, out=None, stream=None, return_lse: bool = False):
     """Attention over a whole prompt: q [1,S,32,128], k/v [1,S,8,128] bf16.
 
     Returns ``out`` [1,S,32,128] bf16 (allocated if not given), enqueued on
-    ``stream`` (default: torch's current stream).
+    ``stream`` (default: torch's current stream).  With ``return_lse`` it
+    returns ``(out, lse)``, lse [1,32,S] fp32 = ln sum_j exp(score_ij).
     """
     import torch
     S = q.shape[1]
@@ -113,13 +116,19 @@ def prefill(q, k, v, causal: bool = True, out=None, stream=None):
     if out is None:
         out = torch.empty_like(q)
     _expect(out, (1, S, HQ, HEAD_DIM), "out")
+    if return_lse:
+        lse = torch.empty((1, HQ, S), dtype=torch.float32, device=q.device)
+        _check("gqa_attn_prefill_lse", lib().gqa_attn_prefill_lse(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), S,
+            1 if causal else 0, _stream(stream)))
+        return out, lse
     _check("gqa_attn_prefill", lib().gqa_attn_prefill(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S,
         1 if causal else 0, _stream(stream)))
     return out
 
 
-def decode(q, kcache, vcache, out=None, workspace=None, stream=None):
+def decode(q, kcache, vcache, out=None, workspace=None, stream=None, return_lse: bool = False):
     """One query token q [1,1,32,128] against kcache/vcache [1,L,8,128] bf16.
 
     With ``workspace`` (a CUDA tensor of at least ``decode_workspace_bytes(L)``
@@ -135,6 +144,14 @@ def decode(q, kcache, vcache, out=None, workspace=None, stream=None):
         out = torch.empty_like(q)
     _expect(out, (1, 1, HQ, HEAD_DIM), "out")
     s = _stream(stream)
+    if return_lse:
+        if workspace is not None:
+            raise ValueError("return_lse uses the library workspace")
+        lse = torch.empty((1, HQ), dtype=torch.float32, device=q.device)
+        _check("gqa_attn_decode_lse", lib().gqa_attn_decode_lse(
+            q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(),
+            lse.data_ptr(), L, s))
+        return out, lse
     if workspace is None:
         _check("gqa_attn_decode", lib().gqa_attn_decode(
             q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(), L, s))

@@ -258,7 +258,7 @@ constexpr int kCmbUnroll = 4;
 __global__ void __launch_bounds__(kCmbWarps * 32)
 decode_combine_kernel(const float *__restrict__ part_o,
                       const float *__restrict__ part_lse, int n_split,
-                      __nv_bfloat16 *__restrict__ out) {
+                      __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
     // Launched as a programmatic dependent of the split kernel: wait until
     // its results are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -316,6 +316,8 @@ decode_combine_kernel(const float *__restrict__ part_o,
         t.x += f * a.x; t.y += f * a.y; t.z += f * a.z; t.w += f * a.w;
     }
     const float inv = 1.f / tden;
+    if (lse != nullptr && lane == 0)  // base-2 chunk values -> natural log
+        lse[h] = (M + __log2f(tden)) * 0.6931471805599453f;
     uint2 pk;
     pk.x = pack_bf16(t.x * inv, t.y * inv);
     pk.y = pack_bf16(t.z * inv, t.w * inv);
@@ -344,7 +346,7 @@ size_t decode_workspace_bytes(const DecodePlan &p) {
 }
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const void *q, void *out, int L, const DecodePlan &plan,
+                          const void *q, void *out, float *lse, int L, const DecodePlan &plan,
                           void *workspace, unsigned *err, cudaStream_t stream) {
     static bool configured[kMaxDevices] = {};  // the attribute is per device
     int dev = 0;
@@ -383,7 +385,7 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel,
                               static_cast<const float *>(part_o),
                               static_cast<const float *>(part_lse), plan.n_split,
-                              static_cast<__nv_bfloat16 *>(out));
+                              static_cast<__nv_bfloat16 *>(out), lse);
 }
 
 }  // namespace gqa

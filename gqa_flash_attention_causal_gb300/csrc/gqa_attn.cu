@@ -186,22 +186,22 @@ gqa_status decode_scratch(DeviceState *dev, void **out) {
     return GQA_OK;
 }
 
-gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, int L,
-                      const gqa::DecodePlan &plan, void *ws, unsigned *err,
+gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, float *lse,
+                      int L, const gqa::DecodePlan &plan, void *ws, unsigned *err,
                       cudaStream_t stream) {
     CUtensorMap kmap, vmap;
     gqa_status st = encode_bshd(&kmap, kc, L, kHkv, gqa::kDecodeBoxRows);
     if (st == GQA_OK) st = encode_bshd(&vmap, vc, L, kHkv, gqa::kDecodeBoxRows);
     if (st != GQA_OK) return st;
-    return from_cuda(gqa::launch_decode(kmap, vmap, q, out, L, plan, ws, err, stream));
+    return from_cuda(gqa::launch_decode(kmap, vmap, q, out, lse, L, plan, ws, err, stream));
 }
 
 }  // namespace
 
 extern "C" {
 
-gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *out, int S,
-                            int causal, cudaStream_t stream) {
+static gqa_status prefill_impl(const void *q, const void *k, const void *v, void *out,
+                               float *lse, int S, int causal, cudaStream_t stream) {
     if (!q || !k || !v || !out) return GQA_ERR_NULL;
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
         return GQA_ERR_ALIGN;
@@ -213,13 +213,26 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
         st = check_device_ptr(p);
         if (st != GQA_OK) return st;
     }
+    if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
     CUtensorMap qmap, kmap, vmap;
     st = encode_bshd(&qmap, q, S, kHq, gqa::kPrefillBoxRows);
     if (st == GQA_OK) st = encode_bshd(&kmap, k, S, kHkv, gqa::kPrefillBoxRows);
     if (st == GQA_OK) st = encode_bshd(&vmap, v, S, kHkv, gqa::kPrefillBoxRows);
     if (st != GQA_OK) return st;
-    return from_cuda(gqa::launch_prefill(qmap, kmap, vmap, out, S, causal ? 1 : 0,
+    return from_cuda(gqa::launch_prefill(qmap, kmap, vmap, out, lse, S, causal ? 1 : 0,
                                          dev->num_sms, dev->err, stream));
+}
+
+gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *out, int S,
+                            int causal, cudaStream_t stream) {
+    return prefill_impl(q, k, v, out, nullptr, S, causal, stream);
+}
+
+gqa_status gqa_attn_prefill_lse(const void *q, const void *k, const void *v, void *out,
+                                float *lse, int S, int causal, cudaStream_t stream) {
+    if (!lse) return GQA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return GQA_ERR_ALIGN;
+    return prefill_impl(q, k, v, out, lse, S, causal, stream);
 }
 
 size_t gqa_attn_decode_workspace_bytes(int L) {
@@ -248,11 +261,11 @@ gqa_status gqa_attn_decode_ws(const void *q, const void *kcache, const void *vca
         return GQA_ERR_WORKSPACE;
     st = check_device_ptr(workspace);
     if (st != GQA_OK) return GQA_ERR_WORKSPACE;
-    return run_decode(q, kcache, vcache, out, L, plan, workspace, dev->err, stream);
+    return run_decode(q, kcache, vcache, out, nullptr, L, plan, workspace, dev->err, stream);
 }
 
-gqa_status gqa_attn_decode(const void *q, const void *kcache, const void *vcache, void *out,
-                           int L, cudaStream_t stream) {
+static gqa_status decode_impl(const void *q, const void *kcache, const void *vcache, void *out,
+                              float *lse, int L, cudaStream_t stream) {
     DeviceState *dev = nullptr;
     gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
     if (st != GQA_OK) return st;
@@ -275,7 +288,20 @@ gqa_status gqa_attn_decode(const void *q, const void *kcache, const void *vcache
             dev->workspace_bytes = bytes;
         }
     }
-    return run_decode(q, kcache, vcache, out, L, plan, dev->workspace, dev->err, stream);
+    if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
+    return run_decode(q, kcache, vcache, out, lse, L, plan, dev->workspace, dev->err, stream);
+}
+
+gqa_status gqa_attn_decode(const void *q, const void *kcache, const void *vcache, void *out,
+                           int L, cudaStream_t stream) {
+    return decode_impl(q, kcache, vcache, out, nullptr, L, stream);
+}
+
+gqa_status gqa_attn_decode_lse(const void *q, const void *kcache, const void *vcache, void *out,
+                               float *lse, int L, cudaStream_t stream) {
+    if (!lse) return GQA_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return GQA_ERR_ALIGN;
+    return decode_impl(q, kcache, vcache, out, lse, L, stream);
 }
 
 gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
@@ -288,7 +314,7 @@ gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache, const void
     void *scratch = nullptr;
     st = decode_scratch(dev, &scratch);
     if (st != GQA_OK) return st;
-    return run_decode(q, kcache, vcache, out, L, plan, scratch, dev->err, stream);
+    return run_decode(q, kcache, vcache, out, nullptr, L, plan, scratch, dev->err, stream);
 }
 
 int gqa_attn_launches_per_call(int is_decode) { return is_decode ? 2 : 1; }

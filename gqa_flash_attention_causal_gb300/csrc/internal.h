@@ -24,8 +24,9 @@ struct DecodePlan {
 DecodePlan decode_plan(int L, int num_sms);
 size_t decode_workspace_bytes(const DecodePlan &p);
 
+// lse (may be null): [32] fp32, natural-log log-sum-exp of each head's scores.
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const void *q, void *out, int L, const DecodePlan &plan,
+                          const void *q, void *out, float *lse, int L, const DecodePlan &plan,
                           void *workspace, unsigned *err, cudaStream_t stream);
 
 // Box sizes the kernels expect in their tensor maps (rows of 64 bf16 each).
@@ -33,8 +34,9 @@ constexpr int kDecodeBoxRows = 64;
 constexpr int kPrefillBoxRows = 128;
 
 // ------------------------------------------------------------------ prefill
+// lse (may be null): [32][S] fp32, natural-log log-sum-exp of each row's scores.
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, void *out, int S, int causal,
+                           const CUtensorMap &vmap, void *out, float *lse, int S, int causal,
                            int num_sms, unsigned *err, cudaStream_t stream);
 
 // ------------------------------------------------------------------ self-test

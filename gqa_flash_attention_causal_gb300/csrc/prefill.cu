@@ -59,6 +59,7 @@ constexpr uint32_t kIdescS = umma_idesc_bf16(kBM, kBN, 0, 0);  // Q.K^T, both K-
 constexpr uint32_t kIdescO = umma_idesc_bf16(kBM, kD, 0, 1);   // P.V, V MN-major
 constexpr float kScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 struct Bars {
     uint32_t base;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, __nv_bfloat16 *__restrict__ out,
-               int S, int causal, unsigned *err) {
+               float *__restrict__ lse, int S, int causal, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -433,6 +434,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             ++o_cnt;
             tc_fence_after();
             const float inv = 1.f / l;
+            if (lse != nullptr && row < S)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
+                lse[size_t(h) * S + row] = (m_run + __log2f(l)) * kLn2;
             __nv_bfloat16 *dst = out + (size_t(row) * kHq + h) * kD;
 #pragma unroll
             for (int c = 0; c < kD / 32; ++c) {
@@ -466,7 +469,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, void *out, int S, int causal,
+                           const CUtensorMap &vmap, void *out, float *lse, int S, int causal,
                            int num_sms, unsigned *err, cudaStream_t stream) {
     static bool configured[kMaxDevices] = {};
     int dev = 0;
@@ -492,7 +495,7 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_kernel, qmap, kmap, vmap,
-                              static_cast<__nv_bfloat16 *>(out), S, causal, err);
+                              static_cast<__nv_bfloat16 *>(out), lse, S, causal, err);
 }
 
 }  // namespace gqa

@@ -66,6 +66,18 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v,
                             void *out, int S, int causal, cudaStream_t stream);
 
 /*
+ * gqa_attn_prefill that also returns, for every query row and head, the
+ * natural-log log-sum-exp of that row's scaled scores,
+ *     lse[h][i] = ln sum_{j in J(i)} exp( q[i,h,:] . k[j,g,:] / sqrt(128) ),
+ * the normaliser of the softmax (what a backward pass or a merge of
+ * attention over separate key ranges needs).  lse: [32][S] fp32 device
+ * memory, 4-byte aligned, written only for rows < S.
+ */
+gqa_status gqa_attn_prefill_lse(const void *q, const void *k, const void *v,
+                                void *out, float *lse, int S, int causal,
+                                cudaStream_t stream);
+
+/*
  * Decode: one query token against a KV cache of length L (every cached
  * position is attended).  q, out: [1][1][32][128] bf16; kcache, vcache:
  * [1][L][8][128] bf16; 1 <= L <= 2^26.
@@ -80,6 +92,12 @@ gqa_status gqa_attn_decode(const void *q, const void *kcache,
                            const void *vcache, void *out, int L,
                            cudaStream_t stream);
 
+/* gqa_attn_decode that also returns lse[h] = ln sum_j exp(q[h,:] . k[j,g,:] /
+ * sqrt(128)) for the 32 query heads: [32] fp32 device memory, 4-byte aligned. */
+gqa_status gqa_attn_decode_lse(const void *q, const void *kcache,
+                               const void *vcache, void *out, float *lse, int L,
+                               cudaStream_t stream);
+
 /* Bytes of device workspace gqa_attn_decode_ws needs for length L (0 if L
  * is out of range). */
 size_t gqa_attn_decode_workspace_bytes(int L);
@@ -87,8 +105,8 @@ size_t gqa_attn_decode_workspace_bytes(int L);
 /*
  * gqa_attn_decode with a caller-owned device workspace of at least
  * gqa_attn_decode_workspace_bytes(L) bytes, 16-byte aligned.  Allocates
- * nothing, so it may be captured in a CUDA graph.  The workspace must not be
- * used by anything else until the call has completed on `stream`.
+ * nothing, so it may be captured in a CUDA graph (tested).  The workspace
+ * must not be used by anything else until the call has completed on `stream`.
  */
 gqa_status gqa_attn_decode_ws(const void *q, const void *kcache,
                               const void *vcache, void *out, int L,
