@@ -31,6 +31,7 @@ SIGNATURES = {
     "gqa_attn_prefill": (_I, [_P, _P, _P, _P, _I, _I, _P]),
     "gqa_attn_prefill_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "gqa_attn_decode_lse": (_I, [_P, _P, _P, _P, _P, _I, _P]),
+    "gqa_attn_prefill_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_workspace_bytes": (_S, [_I]),
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
@@ -126,6 +127,31 @@ def prefill(q, k, v, causal: bool = True, out=None, stream=None, return_lse: boo
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S,
         1 if causal else 0, _stream(stream)))
     return out
+
+
+def prefill_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True, out=None,
+                   stream=None, return_lse: bool = False):
+    """Prefill of sequences packed along dim 0: q [total,32,128], k/v
+    [total,8,128] bf16; sequence s is rows cu_seqlens[s]:cu_seqlens[s+1]
+    (int32 CUDA tensor of batch+1 offsets).  Returns out [total,32,128] (and
+    lse [32,total] fp32 with ``return_lse``)."""
+    import torch
+    total = q.shape[0]
+    _expect(q, (total, HQ, HEAD_DIM), "q")
+    _expect(k, (total, HKV, HEAD_DIM), "k")
+    _expect(v, (total, HKV, HEAD_DIM), "v")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise TypeError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    batch = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, (total, HQ, HEAD_DIM), "out")
+    lse = torch.empty((HQ, total), dtype=torch.float32, device=q.device) if return_lse else None
+    _check("gqa_attn_prefill_varlen", lib().gqa_attn_prefill_varlen(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, cu_seqlens.data_ptr(), batch,
+        int(max_seqlen), total, 1 if causal else 0, _stream(stream)))
+    return (out, lse) if return_lse else out
 
 
 def decode(q, kcache, vcache, out=None, workspace=None, stream=None, return_lse: bool = False):

@@ -29,6 +29,7 @@ namespace {
 __device__ unsigned g_device_error;
 
 constexpr int kMaxPrefillLen = 1 << 20;
+constexpr int kMaxPrefillTotal = 1 << 24;  // rows of a packed batch
 constexpr int kMaxDecodeLen = 1 << 26;
 
 struct DeviceState {
@@ -200,12 +201,21 @@ gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, 
 
 extern "C" {
 
+// Shared by every prefill entry: B packed sequences over `total` rows (cu
+// null: one sequence of `total` rows).
 static gqa_status prefill_impl(const void *q, const void *k, const void *v, void *out,
-                               float *lse, int S, int causal, cudaStream_t stream) {
+                               float *lse, const int *cu, int B, int max_len, int total,
+                               int causal, cudaStream_t stream) {
     if (!q || !k || !v || !out) return GQA_ERR_NULL;
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
         return GQA_ERR_ALIGN;
-    if (S < 1 || S > kMaxPrefillLen) return GQA_ERR_SHAPE;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return GQA_ERR_ALIGN;
+    if (cu && (reinterpret_cast<uintptr_t>(cu) & 3u)) return GQA_ERR_ALIGN;
+    if (B < 1 || max_len < 1 || max_len > kMaxPrefillLen || total < 1 ||
+        total > kMaxPrefillTotal)
+        return GQA_ERR_SHAPE;
+    const long long blocks = ((max_len + 127) / 128 + 1) / 2;
+    if (blocks * B * kHq > 0x7fffffffLL) return GQA_ERR_SHAPE;
     DeviceState *dev = nullptr;
     gqa_status st = current_device(&dev);
     if (st != GQA_OK) return st;
@@ -214,25 +224,34 @@ static gqa_status prefill_impl(const void *q, const void *k, const void *v, void
         if (st != GQA_OK) return st;
     }
     if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
+    if (cu && (st = check_device_ptr(cu)) != GQA_OK) return st;
     CUtensorMap qmap, kmap, vmap;
-    st = encode_bshd(&qmap, q, S, kHq, gqa::kPrefillBoxRows);
-    if (st == GQA_OK) st = encode_bshd(&kmap, k, S, kHkv, gqa::kPrefillBoxRows);
-    if (st == GQA_OK) st = encode_bshd(&vmap, v, S, kHkv, gqa::kPrefillBoxRows);
+    st = encode_bshd(&qmap, q, total, kHq, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&kmap, k, total, kHkv, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, v, total, kHkv, gqa::kPrefillBoxRows);
     if (st != GQA_OK) return st;
-    return from_cuda(gqa::launch_prefill(qmap, kmap, vmap, out, lse, S, causal ? 1 : 0,
-                                         dev->num_sms, dev->err, stream));
+    return from_cuda(gqa::launch_prefill(qmap, kmap, vmap, out, lse, cu, B, max_len, total,
+                                         causal ? 1 : 0, dev->num_sms, dev->err, stream));
 }
 
 gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *out, int S,
                             int causal, cudaStream_t stream) {
-    return prefill_impl(q, k, v, out, nullptr, S, causal, stream);
+    return prefill_impl(q, k, v, out, nullptr, nullptr, 1, S, S, causal, stream);
 }
 
 gqa_status gqa_attn_prefill_lse(const void *q, const void *k, const void *v, void *out,
                                 float *lse, int S, int causal, cudaStream_t stream) {
     if (!lse) return GQA_ERR_NULL;
-    if (reinterpret_cast<uintptr_t>(lse) & 3u) return GQA_ERR_ALIGN;
-    return prefill_impl(q, k, v, out, lse, S, causal, stream);
+    return prefill_impl(q, k, v, out, lse, nullptr, 1, S, S, causal, stream);
+}
+
+gqa_status gqa_attn_prefill_varlen(const void *q, const void *k, const void *v, void *out,
+                                   float *lse, const int *cu_seqlens, int batch,
+                                   int max_seqlen, int total, int causal,
+                                   cudaStream_t stream) {
+    if (!cu_seqlens) return GQA_ERR_NULL;
+    return prefill_impl(q, k, v, out, lse, cu_seqlens, batch, max_seqlen, total, causal,
+                        stream);
 }
 
 size_t gqa_attn_decode_workspace_bytes(int L) {

@@ -34,9 +34,13 @@ constexpr int kDecodeBoxRows = 64;
 constexpr int kPrefillBoxRows = 128;
 
 // ------------------------------------------------------------------ prefill
-// lse (may be null): [32][S] fp32, natural-log log-sum-exp of each row's scores.
+// B packed sequences, sequence s at rows cu_seqlens[s] .. cu_seqlens[s+1]-1 of
+// `total` rows (cu_seqlens null: one sequence of `total` rows); max_len bounds
+// every sequence's length.  lse (may be null): [32][total] fp32, natural-log
+// log-sum-exp of each row's scores.
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, void *out, float *lse, int S, int causal,
+                           const CUtensorMap &vmap, void *out, float *lse,
+                           const int *cu_seqlens, int B, int max_len, int total, int causal,
                            int num_sms, unsigned *err, cudaStream_t stream);
 
 // ------------------------------------------------------------------ self-test

@@ -72,28 +72,57 @@ struct Bars {
     __device__ uint32_t o_full(int t) const { return base + 48 + 16 * kStages + 8 * t; }
 };
 
-// Work decomposition shared by every role: item idx -> (block b, head h),
-// blocks with the most KV tiles first, the 4 heads of a KV group adjacent.
+// Work decomposition shared by every role.  The batch is B packed
+// sequences (sequence s spans rows cu[s] .. cu[s+1]-1 of q, k, v and out;
+// B = 1 with no cu array is the single-sequence case).  Item idx -> (block
+// b of 256 rows, sequence, head): blocks with the most KV tiles first, the
+// heads of one sequence adjacent (the 4 heads of a KV group share K/V in L2).
+// Items whose block lies past the end of their sequence are skipped by every
+// role alike.
+struct Item {
+    int b, h, start, len, T;
+};
+
 struct Work {
-    int S, T, n_blocks, n_items, causal;
-    __device__ Work(int S_, int causal_) : S(S_), causal(causal_) {
-        T = (S + kBM - 1) / kBM;
-        n_blocks = (T + 1) / 2;
-        n_items = n_blocks * kHq;
+    const int *cu;
+    int B, total, n_blocks, n_items, causal;
+    __device__ Work(const int *cu_, int B_, int max_len, int total_, int causal_)
+        : cu(cu_), B(B_), total(total_), causal(causal_) {
+        n_blocks = ((max_len + kBM - 1) / kBM + 1) / 2;
+        n_items = n_blocks * B * kHq;
     }
     // Item of round `r` for CTA `c` (snake order over the grid).
     __device__ int item(int r, int c, int G) const {
         return r * G + ((r & 1) ? (G - 1 - c) : c);
     }
-    __device__ void coords(int idx, int &b, int &h) const {
-        b = causal ? n_blocks - 1 - idx / kHq : idx / kHq;
-        h = idx % kHq;
+    // false: nothing to do for this item (past its sequence, or a malformed
+    // cu array, which also sets kErrBadSeqlens)
+    __device__ bool resolve(int idx, Item &it, unsigned *err) const {
+        const int per_block = B * kHq;
+        it.b = causal ? n_blocks - 1 - idx / per_block : idx / per_block;
+        const int rem = idx % per_block;
+        const int seq = rem / kHq;
+        it.h = rem % kHq;
+        if (cu != nullptr) {
+            it.start = __ldg(cu + seq);
+            it.len = __ldg(cu + seq + 1) - it.start;
+        } else {
+            it.start = 0;
+            it.len = total;
+        }
+        if (it.start < 0 || it.len < 0 || it.start + it.len > total ||
+            it.len > n_blocks * 2 * kBM) {
+            atomicOr(err, kErrBadSeqlens);
+            return false;
+        }
+        it.T = (it.len + kBM - 1) / kBM;
+        return 2 * it.b < it.T;
     }
-    // KV tiles visited by tile t (0 = A, 1 = B) of block b.
-    __device__ int n_kv(int b, int t) const {
-        if (!causal) return T;
-        const int n = 2 * b + t + 1;
-        return n < T ? n : T;
+    // KV tiles visited by tile t (0 = A, 1 = B) of the item.
+    __device__ int n_kv(const Item &it, int t) const {
+        if (!causal) return it.T;
+        const int n = 2 * it.b + t + 1;
+        return n < it.T ? n : it.T;
     }
 };
 
@@ -147,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, __nv_bfloat16 *__restrict__ out,
-               float *__restrict__ lse, int S, int causal, unsigned *err) {
+               float *__restrict__ lse, const int *__restrict__ cu_seqlens, int B,
+               int max_len, int total, int causal, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,7 +188,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const Bars bars{smem_u32(bar_mem)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Work work(S, causal);
+    const Work work(cu_seqlens, B, max_len, total, causal);
     const int G = gridDim.x, cta = blockIdx.x;
 
     if (threadIdx.x == 0) {
@@ -203,23 +233,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             const uint64_t pol_kv = policy_evict_last();
             int kv = 0;
             bool ok = true;
-            for (int r = 0, n = 0; ok; ++r, ++n) {
+            for (int r = 0, n = 0; ok; ++r) {
                 const int idx = work.item(r, cta, G);
                 if (idx >= work.n_items) break;
-                int b, h;
-                work.coords(idx, b, h);
-                const int g = h / kGroup;
+                Item it;
+                if (!work.resolve(idx, it, err)) continue;
+                const int h = it.h, g = h / kGroup;
                 if (n > 0 && !(ok = lone_wait(bars.q_empty(), (n - 1) & 1, err,
                                               kErrWaitEmpty, abort)))
                     break;
+                ++n;
                 mbar_arrive_expect_tx(bars.q_full(), kQBytes);
                 for (int t = 0; t < kTiles; ++t) {
-                    const int row = (2 * b + t) * kBM;
+                    const int row = it.start + (2 * it.b + t) * kBM;
                     const uint32_t dst = sQ + t * kTileBytes;
                     tma_load_3d(dst, &qmap, bars.q_full(), 0, h, row, pol_q);
                     tma_load_3d(dst + kHalfBytes, &qmap, bars.q_full(), 64, h, row, pol_q);
                 }
-                const int nkv = work.n_kv(b, 1);
+                const int nkv = work.n_kv(it, 1);
                 for (int j = 0; j < nkv && ok; ++j) {
                     for (int which = 0; which < 2; ++which, ++kv) {
                         const int s = kv % kStages;
@@ -230,9 +261,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                         const CUtensorMap *m = which ? &vmap : &kmap;
                         const uint32_t dst = sRing + s * kTileBytes;
                         mbar_arrive_expect_tx(bars.kv_full(s), kTileBytes);
-                        tma_load_3d(dst, m, bars.kv_full(s), 0, g, j * kBN, pol_kv);
-                        tma_load_3d(dst + kHalfBytes, m, bars.kv_full(s), 64, g, j * kBN,
-                                    pol_kv);
+                        const int krow = it.start + j * kBN;
+                        tma_load_3d(dst, m, bars.kv_full(s), 0, g, krow, pol_kv);
+                        tma_load_3d(dst + kHalfBytes, m, bars.kv_full(s), 64, g, krow, pol_kv);
                     }
                 }
             }
@@ -264,13 +295,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     umma_ts(d, p + kk * 8, vdesc(vtile, kk), kIdescO, (!first || kk > 0));
                 umma_commit(bars.o_full(t));
             };
-            for (int r = 0, n = 0; ok; ++r, ++n) {
+            for (int r = 0, n = 0; ok; ++r) {
                 const int idx = work.item(r, cta, G);
                 if (idx >= work.n_items) break;
-                int b, h;
-                work.coords(idx, b, h);
-                const int nA = work.n_kv(b, 0), nB = work.n_kv(b, 1);
+                Item it;
+                if (!work.resolve(idx, it, err)) continue;
+                const int nA = work.n_kv(it, 0), nB = work.n_kv(it, 1);
                 if (!(ok = lone_wait(bars.q_full(), n & 1, err, kErrWaitFull, abort))) break;
+                ++n;
                 tc_fence_after();
                 // K_0 -> S_A(0), S_B(0)
                 int kslot = kv % kStages;
@@ -332,11 +364,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int rr = 0; ok; ++rr) {
             const int idx = work.item(rr, cta, G);
             if (idx >= work.n_items) break;
-            int b, h;
-            work.coords(idx, b, h);
-            const int qt = 2 * b + t;
-            const int n = work.n_kv(b, t);
-            const int row = qt * kBM + r;
+            Item it;
+            if (!work.resolve(idx, it, err)) continue;
+            const int h = it.h, len = it.len;
+            const int qt = 2 * it.b + t;
+            const int n = work.n_kv(it, t);
+            const int row = qt * kBM + r;  // row inside the sequence
             float m_run = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 if (!(ok = warp_wait(bars.s_full(t), s_cnt & 1, err, kErrWaitMma, abort)))
@@ -350,7 +383,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 tmem_wait_ld();
                 // keys kbase + c with c <= lim are visible to this row
                 const int kbase = j * kBN;
-                int lim = S - 1 - kbase;
+                int lim = len - 1 - kbase;
                 if (causal && row - kbase < lim) lim = row - kbase;
                 if (lim < kBN - 1) {
 #pragma unroll
@@ -434,9 +467,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             ++o_cnt;
             tc_fence_after();
             const float inv = 1.f / l;
-            if (lse != nullptr && row < S)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
-                lse[size_t(h) * S + row] = (m_run + __log2f(l)) * kLn2;
-            __nv_bfloat16 *dst = out + (size_t(row) * kHq + h) * kD;
+            if (lse != nullptr && row < len)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
+                lse[size_t(h) * total + it.start + row] = (m_run + __log2f(l)) * kLn2;
+            __nv_bfloat16 *dst = out + (size_t(it.start + row) * kHq + h) * kD;
 #pragma unroll
             for (int c = 0; c < kD / 32; ++c) {
                 uint32_t ov[32];
@@ -447,7 +480,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv,
                                       __uint_as_float(ov[2 * e + 1]) * inv);
-                if (row < S) {
+                if (row < len) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -469,7 +502,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, void *out, float *lse, int S, int causal,
+                           const CUtensorMap &vmap, void *out, float *lse,
+                           const int *cu_seqlens, int B, int max_len, int total, int causal,
                            int num_sms, unsigned *err, cudaStream_t stream) {
     static bool configured[kMaxDevices] = {};
     int dev = 0;
@@ -481,9 +515,8 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const int T = (S + kBM - 1) / kBM;
-    const int n_items = (T + 1) / 2 * kHq;
-    const int grid = n_items < num_sms ? n_items : num_sms;
+    const long long n_items = ((max_len + kBM - 1) / kBM + 1) / 2 * (long long)B * kHq;
+    const int grid = n_items < num_sms ? int(n_items) : num_sms;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -495,7 +528,8 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_kernel, qmap, kmap, vmap,
-                              static_cast<__nv_bfloat16 *>(out), lse, S, causal, err);
+                              static_cast<__nv_bfloat16 *>(out), lse, cu_seqlens, B, max_len,
+                              total, causal, err);
 }
 
 }  // namespace gqa

@@ -16,6 +16,7 @@ enum : unsigned {
     kErrWaitMma = 1u << 2,     // waited too long for a tcgen05 MMA commit
     kErrWaitSoftmax = 1u << 3, // MMA issuer waited too long for P
     kErrTmemAlloc = 1u << 4,   // TMEM allocation returned an unusable address
+    kErrBadSeqlens = 1u << 5,  // sequence offsets/lengths outside the tensors
 };
 
 // About one second at the GB300's 2.07 GHz maximum SM clock.

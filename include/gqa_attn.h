@@ -78,6 +78,25 @@ gqa_status gqa_attn_prefill_lse(const void *q, const void *k, const void *v,
                                 cudaStream_t stream);
 
 /*
+ * Prefill of a batch of `batch` independent sequences packed along the
+ * sequence axis (the layout variable-length serving uses): sequence s
+ * occupies rows cu_seqlens[s] .. cu_seqlens[s+1]-1 of
+ *     q, out [total][32][128] bf16,   k, v [total][8][128] bf16,
+ * and attends only within itself (causal or not).  cu_seqlens: batch+1
+ * non-decreasing int32 offsets in DEVICE memory with cu_seqlens[0] = 0 and
+ * cu_seqlens[batch] = total; max_seqlen (host) >= every sequence's length,
+ * <= 2^20; total <= 2^24.  lse (may be NULL): [32][total] fp32, natural-log
+ * log-sum-exp of every row, as gqa_attn_prefill_lse.  A sequence whose
+ * offsets fall outside [0, total] or whose length exceeds max_seqlen is not
+ * computed and sets bit 5 of the device error word (gqa_attn_device_error).
+ * With batch = 1 and cu_seqlens = {0, S} it computes gqa_attn_prefill.
+ */
+gqa_status gqa_attn_prefill_varlen(const void *q, const void *k, const void *v,
+                                   void *out, float *lse, const int *cu_seqlens,
+                                   int batch, int max_seqlen, int total, int causal,
+                                   cudaStream_t stream);
+
+/*
  * Decode: one query token against a KV cache of length L (every cached
  * position is attended).  q, out: [1][1][32][128] bf16; kcache, vcache:
  * [1][L][8][128] bf16; 1 <= L <= 2^26.

@@ -1,0 +1,88 @@
+"""Packed variable-length prefill (batch > 1) against the fp64 oracle, one
+sequence at a time."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_flash_attention_causal_gb300 as gqa
+import oracle
+from gqa_flash_attention_causal_gb300.inputs import normal_bf16, prefill_inputs
+from tests.parity import assert_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def packed(lengths, seed=7, stress=False):
+    total = sum(lengths)
+    mq, mv = (8.0, 100.0) if stress else (1.0, 1.0)
+    q = normal_bf16((total, 32, 128), seed, mq)
+    k = normal_bf16((total, 8, 128), seed + 1, mq)
+    v = normal_bf16((total, 8, 128), seed + 2, mv)
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32)
+    return q, k, v, cu
+
+
+def run(q, k, v, cu, max_len, causal=True, lse=False):
+    out = torch.full((q.shape[0], 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    res = gqa.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), max_len, causal=causal,
+                             out=out, return_lse=lse)
+    torch.cuda.synchronize()
+    return res
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_matches_oracle_per_sequence(causal):
+    lengths = [1, 129, 700, 1000, 3, 256, 0, 300]
+    q, k, v, cu = packed(lengths)
+    out, lse = run(q, k, v, cu, max(lengths), causal=causal, lse=True)
+    assert gqa.device_error() == 0
+    for s, n in enumerate(lengths):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if n == 0:
+            continue
+        want, want_lse = oracle.prefill(q[a:b], k[a:b], v[a:b], causal=causal, with_lse=True)
+        assert_close(out[a:b].cpu(), want, what=f"seq {s} (len {n})")
+        got_lse = lse[:, a:b].cpu().numpy().T
+        assert np.all(np.abs(got_lse - want_lse) <= 1e-3 + 1e-5 * np.abs(want_lse))
+
+
+def test_varlen_single_sequence_equals_dense_prefill():
+    S = 3001
+    q, k, v = prefill_inputs(S)
+    dense = gqa.prefill(q.cuda(), k.cuda(), v.cuda())
+    cu = torch.tensor([0, S], dtype=torch.int32)
+    var = run(q[0], k[0], v[0], cu, S)
+    assert torch.equal(dense[0], var)
+
+
+def test_varlen_long_mixed_batch_sampled():
+    lengths = [4096, 300, 2048, 17, 5000]
+    q, k, v, cu = packed(lengths, seed=21, stress=True)
+    out = run(q, k, v, cu, max(lengths))
+    assert gqa.device_error() == 0
+    for s, n in enumerate(lengths):
+        a = int(cu[s])
+        rows = sample_rows(n, n_random=8, seed=s)
+        want = oracle.prefill_rows(q[a:a + n], k[a:a + n], v[a:a + n], rows)
+        scale = float(v[a:a + n].float().abs().max())
+        assert_close(out[a:a + n][rows].cpu(), want, scale=scale, what=f"seq {s}")
+
+
+def test_varlen_sequence_longer_than_max_is_flagged_not_computed():
+    lengths = [100, 2000, 100]
+    q, k, v, cu = packed(lengths, seed=31)
+    out = run(q, k, v, cu, 1000)   # the middle sequence exceeds max_seqlen's blocks
+    flags = gqa.device_error()
+    assert flags & (1 << 5)
+    for s in (0, 2):
+        a, b = int(cu[s]), int(cu[s + 1])
+        assert_close(out[a:b].cpu(), oracle.prefill(q[a:b], k[a:b], v[a:b]), what=f"seq {s}")
+    assert bool(torch.isnan(out[100:2100].float()).all())  # untouched
+
+
+def test_varlen_rejects_bad_host_arguments():
+    q, k, v, cu = packed([10, 20])
+    with pytest.raises(TypeError):
+        gqa.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda().long(), 20)
+    with pytest.raises(gqa.GqaError):
+        gqa.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), 0)
