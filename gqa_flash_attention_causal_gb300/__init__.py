@@ -32,6 +32,7 @@ SIGNATURES = {
     "gqa_attn_prefill_lse": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "gqa_attn_decode_lse": (_I, [_P, _P, _P, _P, _P, _I, _P]),
     "gqa_attn_prefill_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "gqa_attn_decode_batched": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_workspace_bytes": (_S, [_I]),
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
@@ -187,6 +188,30 @@ def decode(q, kcache, vcache, out=None, workspace=None, stream=None, return_lse:
             q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(), L,
             workspace.data_ptr(), nbytes, s))
     return out
+
+
+def decode_batched(q, kcache, vcache, seqlens=None, out=None, stream=None,
+                   return_lse: bool = False):
+    """Decode of a batch: q [B,32,128] against caches [B,Lmax,8,128] bf16;
+    sequence b attends to its first seqlens[b] rows (int32 CUDA tensor [B];
+    None = all Lmax).  Returns out [B,32,128] (and lse [B,32] fp32)."""
+    import torch
+    B, Lmax = kcache.shape[0], kcache.shape[1]
+    _expect(q, (B, HQ, HEAD_DIM), "q")
+    _expect(kcache, (B, Lmax, HKV, HEAD_DIM), "kcache")
+    _expect(vcache, (B, Lmax, HKV, HEAD_DIM), "vcache")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or not seqlens.is_cuda
+                                or tuple(seqlens.shape) != (B,)):
+        raise TypeError("seqlens must be an int32 CUDA tensor of shape [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, (B, HQ, HEAD_DIM), "out")
+    lse = torch.empty((B, HQ), dtype=torch.float32, device=q.device) if return_lse else None
+    _check("gqa_attn_decode_batched", lib().gqa_attn_decode_batched(
+        q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None,
+        seqlens.data_ptr() if seqlens is not None else None, B, Lmax, _stream(stream)))
+    return (out, lse) if return_lse else out
 
 
 def decode_noalloc(q, kcache, vcache, out, stream=None):

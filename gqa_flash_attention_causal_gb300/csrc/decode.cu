@@ -47,9 +47,9 @@ constexpr float kScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
-                    const __nv_bfloat16 *__restrict__ q, int L, int chunk,
-                    float *__restrict__ part_o, float *__restrict__ part_lse,
-                    unsigned *err) {
+                    const __nv_bfloat16 *__restrict__ q, const int *__restrict__ seqlens,
+                    int Lmax, int chunk, float *__restrict__ part_o,
+                    float *__restrict__ part_lse, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -60,11 +60,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t tiles = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
 
-    const int split = blockIdx.x, g = blockIdx.y;
-    const int key0 = split * chunk;
-    const int key_end = min(L, key0 + chunk);
-    const int n_iter = (key_end - key0 + kStageKeys - 1) / kStageKeys;
+    const int split = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
+    const int n_split = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // this CTA's chunk of sequence `seq`, whose cache holds rows
+    // seq*Lmax .. seq*Lmax + L - 1 of the tensor maps
+    const int row0 = seq * Lmax;
+    q += size_t(seq) * kHq * kD;
+    part_o += size_t(seq) * n_split * kHq * kD;
+    part_lse += size_t(seq) * n_split * kHq;
 
     // Let the combine kernel (a programmatic dependent) get scheduled now; it
     // still waits for this whole grid to finish before reading its results.
@@ -84,8 +88,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncthreads();
     // Launched as a programmatic dependent of whatever kernel precedes it on
     // the stream: everything above overlapped that kernel's tail; from here
-    // on its results (q, the caches) are complete and visible.
+    // on its results (q, the caches, the lengths) are complete and visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    int L = Lmax;
+    if (seqlens != nullptr) {
+        L = __ldg(seqlens + seq);
+        if (L < 1 || L > Lmax) {  // not computed; the combine skips it too
+            if (threadIdx.x == 0) atomicOr(err, kErrBadSeqlens);
+            L = 0;
+        }
+    }
+    const int key0 = split * chunk;
+    const int key_end = min(L, key0 + chunk);
+    const int n_iter = key_end > key0 ? (key_end - key0 + kStageKeys - 1) / kStageKeys : 0;
 
     if (warp == kWarps) {
         // ---------------------------------------------------- TMA producer
@@ -97,7 +112,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     !mbar_wait(empty0 + 8 * s, ((it / kStages) & 1) ^ 1, err, kErrWaitEmpty))
                     break;
                 const uint32_t full = full0 + 8 * s, dst = tiles + s * kStageBytes;
-                const int row = key0 + it * kStageKeys;
+                const int row = row0 + key0 + it * kStageKeys;
                 mbar_arrive_expect_tx(full, kStageBytes);
                 tma_load_3d(dst, &kmap, full, 0, g, row, pol);
                 tma_load_3d(dst + kHalfBytes, &kmap, full, 64, g, row, pol);
@@ -196,6 +211,16 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
 
+    if (n_iter == 0) {  // no keys here: a partial that carries no weight
+        const int t = threadIdx.x;
+        const int n = t >> 5, d0 = (t & 31) * 4;
+        const int hq = g * kGroup + n;
+        *reinterpret_cast<float4 *>(part_o + (size_t(split) * kHq + hq) * kD + d0) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+        if (d0 == 0) part_lse[split * kHq + hq] = -INFINITY;
+        return;
+    }
+
     // ------------------------------------------- merge the 4 warps' states
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -258,13 +283,23 @@ constexpr int kCmbUnroll = 4;
 __global__ void __launch_bounds__(kCmbWarps * 32)
 decode_combine_kernel(const float *__restrict__ part_o,
                       const float *__restrict__ part_lse, int n_split,
-                      __nv_bfloat16 *__restrict__ out, float *__restrict__ lse) {
+                      __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
+                      const int *__restrict__ seqlens, int Lmax) {
     // Launched as a programmatic dependent of the split kernel: wait until
     // its results are visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float s_m[kCmbWarps], s_den[kCmbWarps];
     __shared__ float4 s_acc[kCmbWarps][32];
-    const int h = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x, seq = blockIdx.y;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (seqlens != nullptr) {
+        const int L = __ldg(seqlens + seq);
+        if (L < 1 || L > Lmax) return;  // flagged by the split kernel; out untouched
+    }
+    part_o += size_t(seq) * n_split * kHq * kD;
+    part_lse += size_t(seq) * n_split * kHq;
+    out += size_t(seq) * kHq * kD;
+    if (lse != nullptr) lse += size_t(seq) * kHq;
     const int d0 = lane * 4;
     float m = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -283,6 +318,7 @@ decode_combine_kernel(const float *__restrict__ part_o,
 #pragma unroll
         for (int u = 0; u < kCmbUnroll; ++u) {
             if (s0 + u * kCmbWarps >= n_split) break;
+            if (l[u] == -INFINITY) continue;  // a chunk past the sequence's end
             if (l[u] > m) {
                 const float sc = ex2(m - l[u]);  // 0 while m is -inf
                 den *= sc;
@@ -326,28 +362,32 @@ decode_combine_kernel(const float *__restrict__ part_o,
 
 }  // namespace
 
-DecodePlan decode_plan(int L, int num_sms) {
-    const int max_split = (L + kStageKeys - 1) / kStageKeys;
-    int n = num_sms * kCtasPerSm / kHkv;  // one wave of (split, head) CTAs
+DecodePlan decode_plan(int Lmax, int batch, int num_sms) {
+    const int max_split = (Lmax + kStageKeys - 1) / kStageKeys;
+    // one wave of (split, KV head, sequence) CTAs
+    int n = num_sms * kCtasPerSm / (kHkv * batch);
     if (n < 1) n = 1;
     if (n > max_split) n = max_split;
-    int chunk = (L + n - 1) / n;
+    int chunk = (Lmax + n - 1) / n;
     chunk = (chunk + kStageKeys - 1) / kStageKeys * kStageKeys;
     DecodePlan p;
     p.chunk = chunk;
-    p.n_split = (L + chunk - 1) / chunk;
+    p.n_split = (Lmax + chunk - 1) / chunk;
+    p.batch = batch;
     return p;
 }
 
 size_t decode_workspace_bytes(const DecodePlan &p) {
-    const size_t o = size_t(p.n_split) * kHq * kD * sizeof(float);
-    const size_t lse = size_t(p.n_split) * kHq * sizeof(float);
+    const size_t parts = size_t(p.n_split) * p.batch;
+    const size_t o = parts * kHq * kD * sizeof(float);
+    const size_t lse = parts * kHq * sizeof(float);
     return o + ((lse + 255) / 256) * 256;
 }
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const void *q, void *out, float *lse, int L, const DecodePlan &plan,
-                          void *workspace, unsigned *err, cudaStream_t stream) {
+                          const void *q, void *out, float *lse, const int *seqlens, int Lmax,
+                          const DecodePlan &plan, void *workspace, unsigned *err,
+                          cudaStream_t stream) {
     static bool configured[kMaxDevices] = {};  // the attribute is per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -359,7 +399,7 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
         configured[dev] = true;
     }
     float *part_o = static_cast<float *>(workspace);
-    float *part_lse = part_o + size_t(plan.n_split) * kHq * kD;
+    float *part_lse = part_o + size_t(plan.n_split) * plan.batch * kHq * kD;
 
     // Both kernels are programmatic dependents of their predecessor on the
     // stream: their launch and set-up overlap it, and each waits
@@ -368,24 +408,24 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.n_split, kHkv);
+    cfg.gridDim = dim3(plan.n_split, kHkv, plan.batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, decode_split_kernel, kmap, vmap,
-                           static_cast<const __nv_bfloat16 *>(q), L, plan.chunk, part_o,
-                           part_lse, err);
+                           static_cast<const __nv_bfloat16 *>(q), seqlens, Lmax, plan.chunk,
+                           part_o, part_lse, err);
     if (e != cudaSuccess) return e;
 
-    cfg.gridDim = dim3(kHq);
+    cfg.gridDim = dim3(kHq, plan.batch);
     cfg.blockDim = dim3(kCmbWarps * 32);
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel,
                               static_cast<const float *>(part_o),
                               static_cast<const float *>(part_lse), plan.n_split,
-                              static_cast<__nv_bfloat16 *>(out), lse);
+                              static_cast<__nv_bfloat16 *>(out), lse, seqlens, Lmax);
 }
 
 }  // namespace gqa

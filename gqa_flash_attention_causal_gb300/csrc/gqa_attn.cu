@@ -31,6 +31,7 @@ __device__ unsigned g_device_error;
 constexpr int kMaxPrefillLen = 1 << 20;
 constexpr int kMaxPrefillTotal = 1 << 24;  // rows of a packed batch
 constexpr int kMaxDecodeLen = 1 << 26;
+constexpr long long kMaxDecodeRows = 1ll << 30;  // batch x cache rows
 
 struct DeviceState {
     bool probed = false;
@@ -188,13 +189,39 @@ gqa_status decode_scratch(DeviceState *dev, void **out) {
 }
 
 gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, float *lse,
-                      int L, const gqa::DecodePlan &plan, void *ws, unsigned *err,
-                      cudaStream_t stream) {
+                      const int *seqlens, int Lmax, const gqa::DecodePlan &plan, void *ws,
+                      unsigned *err, cudaStream_t stream) {
     CUtensorMap kmap, vmap;
-    gqa_status st = encode_bshd(&kmap, kc, L, kHkv, gqa::kDecodeBoxRows);
-    if (st == GQA_OK) st = encode_bshd(&vmap, vc, L, kHkv, gqa::kDecodeBoxRows);
+    const int rows = Lmax * plan.batch;
+    gqa_status st = encode_bshd(&kmap, kc, rows, kHkv, gqa::kDecodeBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, vc, rows, kHkv, gqa::kDecodeBoxRows);
     if (st != GQA_OK) return st;
-    return from_cuda(gqa::launch_decode(kmap, vmap, q, out, lse, L, plan, ws, err, stream));
+    return from_cuda(gqa::launch_decode(kmap, vmap, q, out, lse, seqlens, Lmax, plan, ws, err,
+                                        stream));
+}
+
+// Library-owned decode workspace of at least `need` bytes on this device
+// (grown with cudaMalloc when a larger batch needs it; never inside capture).
+gqa_status library_workspace(DeviceState *dev, size_t need, void **ws) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (dev->workspace_bytes < need) {
+        // at least the largest single-sequence plan, so batch 1 never regrows
+        const gqa::DecodePlan most = gqa::decode_plan(kMaxDecodeLen, 1, dev->num_sms);
+        size_t bytes = gqa::decode_workspace_bytes(most);
+        if (bytes < need) bytes = need;
+        void *p = nullptr;
+        const cudaError_t e = cudaMalloc(&p, bytes);
+        if (e != cudaSuccess) {
+            note_error("cudaMalloc (decode workspace)", e);
+            cudaGetLastError();
+            return GQA_ERR_CUDA;
+        }
+        if (dev->workspace) cudaFree(dev->workspace);
+        dev->workspace = p;
+        dev->workspace_bytes = bytes;
+    }
+    *ws = dev->workspace;
+    return GQA_OK;
 }
 
 }  // namespace
@@ -258,14 +285,14 @@ size_t gqa_attn_decode_workspace_bytes(int L) {
     if (L < 1 || L > kMaxDecodeLen) return 0;
     DeviceState *dev = nullptr;
     if (current_device(&dev) != GQA_OK) return 0;
-    return gqa::decode_workspace_bytes(gqa::decode_plan(L, dev->num_sms));
+    return gqa::decode_workspace_bytes(gqa::decode_plan(L, 1, dev->num_sms));
 }
 
 int gqa_attn_decode_num_splits(int L) {
     if (L < 1 || L > kMaxDecodeLen) return 0;
     DeviceState *dev = nullptr;
     if (current_device(&dev) != GQA_OK) return 0;
-    return gqa::decode_plan(L, dev->num_sms).n_split;
+    return gqa::decode_plan(L, 1, dev->num_sms).n_split;
 }
 
 gqa_status gqa_attn_decode_ws(const void *q, const void *kcache, const void *vcache,
@@ -274,13 +301,14 @@ gqa_status gqa_attn_decode_ws(const void *q, const void *kcache, const void *vca
     DeviceState *dev = nullptr;
     gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
     if (st != GQA_OK) return st;
-    const gqa::DecodePlan plan = gqa::decode_plan(L, dev->num_sms);
+    const gqa::DecodePlan plan = gqa::decode_plan(L, 1, dev->num_sms);
     if (!workspace || misaligned(workspace) ||
         workspace_bytes < gqa::decode_workspace_bytes(plan))
         return GQA_ERR_WORKSPACE;
     st = check_device_ptr(workspace);
     if (st != GQA_OK) return GQA_ERR_WORKSPACE;
-    return run_decode(q, kcache, vcache, out, nullptr, L, plan, workspace, dev->err, stream);
+    return run_decode(q, kcache, vcache, out, nullptr, nullptr, L, plan, workspace, dev->err,
+                      stream);
 }
 
 static gqa_status decode_impl(const void *q, const void *kcache, const void *vcache, void *out,
@@ -288,27 +316,12 @@ static gqa_status decode_impl(const void *q, const void *kcache, const void *vca
     DeviceState *dev = nullptr;
     gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
     if (st != GQA_OK) return st;
-    const gqa::DecodePlan plan = gqa::decode_plan(L, dev->num_sms);
-    const size_t need = gqa::decode_workspace_bytes(plan);
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (dev->workspace_bytes < need) {
-            // Size for the largest plan this device can produce, once.
-            const gqa::DecodePlan most = gqa::decode_plan(kMaxDecodeLen, dev->num_sms);
-            size_t bytes = gqa::decode_workspace_bytes(most);
-            if (bytes < need) bytes = need;
-            void *p = nullptr;
-            if (cudaMalloc(&p, bytes) != cudaSuccess) {
-                cudaGetLastError();
-                return GQA_ERR_CUDA;
-            }
-            if (dev->workspace) cudaFree(dev->workspace);
-            dev->workspace = p;
-            dev->workspace_bytes = bytes;
-        }
-    }
     if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
-    return run_decode(q, kcache, vcache, out, lse, L, plan, dev->workspace, dev->err, stream);
+    const gqa::DecodePlan plan = gqa::decode_plan(L, 1, dev->num_sms);
+    void *ws = nullptr;
+    st = library_workspace(dev, gqa::decode_workspace_bytes(plan), &ws);
+    if (st != GQA_OK) return st;
+    return run_decode(q, kcache, vcache, out, lse, nullptr, L, plan, ws, dev->err, stream);
 }
 
 gqa_status gqa_attn_decode(const void *q, const void *kcache, const void *vcache, void *out,
@@ -323,17 +336,47 @@ gqa_status gqa_attn_decode_lse(const void *q, const void *kcache, const void *vc
     return decode_impl(q, kcache, vcache, out, lse, L, stream);
 }
 
+gqa_status gqa_attn_decode_batched(const void *q, const void *kcache, const void *vcache,
+                                   void *out, float *lse, const int *seqlens, int batch,
+                                   int max_len, cudaStream_t stream) {
+    if (!q || !kcache || !vcache || !out) return GQA_ERR_NULL;
+    if (misaligned(q) || misaligned(kcache) || misaligned(vcache) || misaligned(out))
+        return GQA_ERR_ALIGN;
+    if ((lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+        (seqlens && (reinterpret_cast<uintptr_t>(seqlens) & 3u)))
+        return GQA_ERR_ALIGN;
+    if (batch < 1 || max_len < 1 || max_len > kMaxDecodeLen ||
+        (long long)batch * max_len > kMaxDecodeRows)
+        return GQA_ERR_SHAPE;
+    DeviceState *dev = nullptr;
+    gqa_status st = current_device(&dev);
+    if (st != GQA_OK) return st;
+    for (const void *p : {q, kcache, vcache, static_cast<const void *>(out)}) {
+        st = check_device_ptr(p);
+        if (st != GQA_OK) return st;
+    }
+    if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
+    if (seqlens && (st = check_device_ptr(seqlens)) != GQA_OK) return st;
+    const gqa::DecodePlan plan = gqa::decode_plan(max_len, batch, dev->num_sms);
+    void *ws = nullptr;
+    st = library_workspace(dev, gqa::decode_workspace_bytes(plan), &ws);
+    if (st != GQA_OK) return st;
+    return run_decode(q, kcache, vcache, out, lse, seqlens, max_len, plan, ws, dev->err,
+                      stream);
+}
+
 gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
                                    void *out, int L, cudaStream_t stream) {
     DeviceState *dev = nullptr;
     gqa_status st = decode_args(q, kcache, vcache, out, L, &dev);
     if (st != GQA_OK) return st;
-    const gqa::DecodePlan plan = gqa::decode_plan(L, dev->num_sms);
+    const gqa::DecodePlan plan = gqa::decode_plan(L, 1, dev->num_sms);
     if (gqa::decode_workspace_bytes(plan) > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;
     void *scratch = nullptr;
     st = decode_scratch(dev, &scratch);
     if (st != GQA_OK) return st;
-    return run_decode(q, kcache, vcache, out, nullptr, L, plan, scratch, dev->err, stream);
+    return run_decode(q, kcache, vcache, out, nullptr, nullptr, L, plan, scratch, dev->err,
+                      stream);
 }
 
 int gqa_attn_launches_per_call(int is_decode) { return is_decode ? 2 : 1; }

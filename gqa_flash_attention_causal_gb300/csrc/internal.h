@@ -14,20 +14,25 @@ constexpr int kD = 128;    // head dim
 constexpr int kMaxDevices = 64;
 
 // ------------------------------------------------------------------ decode
-// Split plan: the KV length is cut into n_split chunks of `chunk` keys (a
-// multiple of the 64-key stage); CTA (split, g) handles chunk `split` of KV
-// head g for its 4 query heads.
+// Split plan: each sequence's cache (Lmax rows) is cut into n_split chunks
+// of `chunk` keys (a multiple of the 64-key stage); CTA (split, g, seq)
+// handles chunk `split` of KV head g of sequence seq for its 4 query heads.
 struct DecodePlan {
     int n_split;
     int chunk;
+    int batch;
 };
-DecodePlan decode_plan(int L, int num_sms);
+DecodePlan decode_plan(int Lmax, int batch, int num_sms);
 size_t decode_workspace_bytes(const DecodePlan &p);
 
-// lse (may be null): [32] fp32, natural-log log-sum-exp of each head's scores.
+// q, out [batch][32][128]; caches [batch][Lmax][8][128] behind the tensor
+// maps; sequence s attends to its first seqlens[s] rows (seqlens null:
+// all Lmax rows).  lse (may be null): [batch][32] fp32 natural-log
+// log-sum-exp.
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          const void *q, void *out, float *lse, int L, const DecodePlan &plan,
-                          void *workspace, unsigned *err, cudaStream_t stream);
+                          const void *q, void *out, float *lse, const int *seqlens, int Lmax,
+                          const DecodePlan &plan, void *workspace, unsigned *err,
+                          cudaStream_t stream);
 
 // Box sizes the kernels expect in their tensor maps (rows of 64 bf16 each).
 constexpr int kDecodeBoxRows = 64;

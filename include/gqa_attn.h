@@ -117,6 +117,24 @@ gqa_status gqa_attn_decode_lse(const void *q, const void *kcache,
                                const void *vcache, void *out, float *lse, int L,
                                cudaStream_t stream);
 
+/*
+ * Decode of a batch: `batch` independent query tokens, sequence s with its
+ * own cache of max_len rows,
+ *     q, out [batch][32][128] bf16,   kcache, vcache [batch][max_len][8][128] bf16,
+ * attending to the first seqlens[s] rows of its cache (1 <= seqlens[s] <=
+ * max_len; seqlens: batch int32 in DEVICE memory, or NULL for all max_len
+ * rows).  lse (may be NULL): [batch][32] fp32 as gqa_attn_decode_lse.
+ * Chunks of every sequence run in one wave across the SMs and are merged
+ * per sequence.  A sequence whose length is outside [1, max_len] is not
+ * computed (its out rows are left untouched) and sets bit 5 of the device
+ * error word.  Uses (and if needed grows) the library-owned workspace of
+ * gqa_attn_decode.  1 <= max_len <= 2^26, batch * max_len <= 2^30.
+ */
+gqa_status gqa_attn_decode_batched(const void *q, const void *kcache,
+                                   const void *vcache, void *out, float *lse,
+                                   const int *seqlens, int batch, int max_len,
+                                   cudaStream_t stream);
+
 /* Bytes of device workspace gqa_attn_decode_ws needs for length L (0 if L
  * is out of range). */
 size_t gqa_attn_decode_workspace_bytes(int L);
