@@ -454,6 +454,73 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def sweep_batch(kind, shape, dev, peaks, src):
+    """Throughput and parity of a packed prefill batch or a batched decode."""
+    import numpy as np
+    import torch
+    import gqa_flash_attention_causal_gb300 as gqa
+    import oracle
+    from gqa_flash_attention_causal_gb300.inputs import normal_bf16
+
+    def med_time(fn, n=5):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    if kind == "varlen":
+        lens = list(shape)
+        total = sum(lens)
+        q = normal_bf16((total, HQ, D), 1)
+        k = normal_bf16((total, HKV, D), 2)
+        v = normal_bf16((total, HKV, D), 3)
+        cu = torch.tensor([0] + np.cumsum(lens).tolist(), dtype=torch.int32, device=dev)
+        dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+        out = torch.empty_like(dq)
+        ms = med_time(lambda: gqa.prefill_varlen(dq, dk, dv, cu, max(lens), out=out))
+        errs = []
+        for s_, n in enumerate(lens):
+            a = int(cu[s_])
+            rows = sorted({0, n - 1, n // 2})
+            want = oracle.prefill_rows(q[a:a + n], k[a:a + n], v[a:a + n], rows)
+            errs.append(np.abs(out[a:a + n][rows].double().cpu().numpy() - want))
+        err = np.concatenate([e.ravel() for e in errs])
+        flops = sum(prefill_flops(n) for n in lens)
+        tput = flops / (ms * 1e-3) / 1e12
+        line = {"workload": "prefill_varlen", "lengths": lens, "ms": ms, "tflops": tput,
+                "frac_of_burst": tput / peaks["bf16_tflops"]}
+    else:
+        B, Lmax = shape
+        q = normal_bf16((B, HQ, D), 1)
+        kc = normal_bf16((B, Lmax, HKV, D), 2)
+        vc = normal_bf16((B, Lmax, HKV, D), 3)
+        dq, dk, dv = q.to(dev), kc.to(dev), vc.to(dev)
+        sl = torch.full((B,), Lmax, dtype=torch.int32, device=dev)
+        out = torch.empty_like(dq)
+        ms = med_time(lambda: gqa.decode_batched(dq, dk, dv, sl, out=out))
+        errs = [np.abs(out[b].double().cpu().numpy() - oracle.decode(q[b], kc[b], vc[b]))
+                for b in (0, B - 1)]
+        err = np.concatenate([e.ravel() for e in errs])
+        nbytes = B * decode_bytes(Lmax)
+        tput = nbytes / (ms * 1e-3) / 1e9
+        line = {"workload": "decode_batched", "batch": B, "L": Lmax, "ms": ms, "gbs": tput,
+                "frac_of_measured_hbm": tput / peaks["hbm_gbs"],
+                "frac_of_8tbs": tput / NORTH_STAR_HBM_GBS,
+                "note": "eager calls; the batch's caches exceed L2"}
+    line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
+                 "parity_ok": bool(err.max() <= 2e-2 and err.mean() <= 2e-3), "peaks": src})
+    if gqa.device_error() != 0:
+        raise RuntimeError("device-side wait timed out")
+    return line
+
+
 def run_sweep(args):
     """One JSON line per configuration of the pages' Result table (plus the
     S=512 and stress cases): GPU time, throughput, fraction of roofline,
@@ -487,7 +554,13 @@ def run_sweep(args):
     cases += [("prefill_full", S, False) for S in (4096, 16384)]
     cases += [("decode", L, False) for L in (2048, 4096, 8192, 16384, 32768, 65536)]
     cases += [("decode", 32768, True)]
+    cases += [("varlen", (4096,) * 8, False), ("varlen", (8192, 4096, 2048, 1024, 512, 256), False)]
+    cases += [("batched", (8, 8192), False), ("batched", (32, 4096), False),
+              ("batched", (128, 2048), False)]
     for kind, n, stress in cases:
+        if kind in ("varlen", "batched"):
+            print(json.dumps(sweep_batch(kind, n, dev, peaks, src)), flush=True)
+            continue
         if kind.startswith("prefill"):
             causal = kind == "prefill"
             q, k, v = prefill_inputs(n, stress=stress)
