@@ -83,6 +83,7 @@ struct Item {
     int b, h, start, len, T;
 };
 
+template <bool kVarlen>
 struct Work {
     const int *cu;
     int B, total, n_blocks, n_items, causal;
@@ -103,17 +104,17 @@ struct Work {
         const int rem = idx % per_block;
         const int seq = rem / kHq;
         it.h = rem % kHq;
-        if (cu != nullptr) {
+        if (kVarlen) {
             it.start = __ldg(cu + seq);
             it.len = __ldg(cu + seq + 1) - it.start;
+            if (it.start < 0 || it.len < 0 || it.start + it.len > total ||
+                it.len > n_blocks * 2 * kBM) {
+                atomicOr(err, kErrBadSeqlens);
+                return false;
+            }
         } else {
             it.start = 0;
             it.len = total;
-        }
-        if (it.start < 0 || it.len < 0 || it.start + it.len > total ||
-            it.len > n_blocks * 2 * kBM) {
-            atomicOr(err, kErrBadSeqlens);
-            return false;
         }
         it.T = (it.len + kBM - 1) / kBM;
         return 2 * it.b < it.T;
@@ -172,6 +173,7 @@ __device__ __forceinline__ uint64_t vdesc(uint32_t tile, int kk) {
     return umma_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
 }
 
+template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap,
@@ -188,7 +190,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const Bars bars{smem_u32(bar_mem)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Work work(cu_seqlens, B, max_len, total, causal);
+    const Work<kVarlen> work(cu_seqlens, B, max_len, total, causal);
     const int G = gridDim.x, cta = blockIdx.x;
 
     if (threadIdx.x == 0) {
@@ -499,19 +501,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     }
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, void *out, float *lse,
-                           const int *cu_seqlens, int B, int max_len, int total, int causal,
-                           int num_sms, unsigned *err, cudaStream_t stream) {
+template <bool kVarlen>
+cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                   void *out, float *lse, const int *cu_seqlens, int B, int max_len, int total,
+                   int causal, int num_sms, unsigned *err, cudaStream_t stream) {
     static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSmemBytes));
+        e = cudaFuncSetAttribute(prefill_kernel<kVarlen>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -527,9 +527,23 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel, qmap, kmap, vmap,
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kVarlen>, qmap, kmap, vmap,
                               static_cast<__nv_bfloat16 *>(out), lse, cu_seqlens, B, max_len,
                               total, causal, err);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, void *out, float *lse,
+                           const int *cu_seqlens, int B, int max_len, int total, int causal,
+                           int num_sms, unsigned *err, cudaStream_t stream) {
+    // one sequence: the instantiation without per-sequence offsets
+    if (cu_seqlens == nullptr)
+        return launch<false>(qmap, kmap, vmap, out, lse, nullptr, 1, total, total, causal,
+                             num_sms, err, stream);
+    return launch<true>(qmap, kmap, vmap, out, lse, cu_seqlens, B, max_len, total, causal,
+                        num_sms, err, stream);
 }
 
 }  // namespace gqa
