@@ -38,6 +38,7 @@ SIGNATURES = {
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
     "gqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_num_splits": (_I, [_I]),
+    "gqa_attn_decode_plan": (_I, [_I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "gqa_attn_launches_per_call": (_I, [_I]),
     "gqa_attn_device_error": (_I, [ctypes.POINTER(ctypes.c_uint), _I]),
     "gqa_attn_status_string": (ctypes.c_char_p, [_I]),
@@ -232,6 +233,15 @@ def decode_noalloc(q, kcache, vcache, out, stream=None):
 
 def decode_workspace_bytes(L: int) -> int:
     return int(lib().gqa_attn_decode_workspace_bytes(int(L)))
+
+
+def decode_plan(L: int, batch: int = 1, num_sms: int = 152):
+    """(n_split, chunk) of the decode for cache length L (host-side, no GPU)."""
+    n, c = ctypes.c_int(0), ctypes.c_int(0)
+    if not lib().gqa_attn_decode_plan(int(L), int(batch), int(num_sms), ctypes.byref(n),
+                                      ctypes.byref(c)):
+        raise ValueError("decode_plan: arguments out of range")
+    return n.value, c.value
 
 
 def decode_num_splits(L: int) -> int:

@@ -288,6 +288,15 @@ size_t gqa_attn_decode_workspace_bytes(int L) {
     return gqa::decode_workspace_bytes(gqa::decode_plan(L, 1, dev->num_sms));
 }
 
+int gqa_attn_decode_plan(int L, int batch, int num_sms, int *n_split, int *chunk) {
+    if (!n_split || !chunk || L < 1 || L > kMaxDecodeLen || batch < 1 || num_sms < 1)
+        return 0;
+    const gqa::DecodePlan p = gqa::decode_plan(L, batch, num_sms);
+    *n_split = p.n_split;
+    *chunk = p.chunk;
+    return 1;
+}
+
 int gqa_attn_decode_num_splits(int L) {
     if (L < 1 || L > kMaxDecodeLen) return 0;
     DeviceState *dev = nullptr;

@@ -177,6 +177,12 @@ gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache,
                                    const void *vcache, void *out, int L,
                                    cudaStream_t stream);
 
+/* The decode's split plan for cache length L, batch and SM count, computed on
+ * the host without touching a device: every sequence's cache is cut into
+ * *n_split chunks of *chunk keys (a multiple of 64).  Returns 1, or 0 on
+ * out-of-range arguments. */
+int gqa_attn_decode_plan(int L, int batch, int num_sms, int *n_split, int *chunk);
+
 /* Number of KV chunks (splits) the decode uses for length L on the current
  * device; 0 if L is out of range.  Exposed for tests and the bench. */
 int gqa_attn_decode_num_splits(int L);

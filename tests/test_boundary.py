@@ -102,3 +102,27 @@ def test_workspace_too_small(lib):
     with pytest.raises(gqa.GqaError) as e:
         gqa.decode(q, kc, kc, workspace=ws)
     assert e.value.code == 5
+
+
+@pytest.mark.parametrize("sms", [152, 148, 132, 8, 1])
+def test_decode_plan_invariants(lib, sms):
+    """The split plan covers every key exactly once, in 64-key multiples,
+    and uses at most one wave of (split, KV head, sequence) CTAs."""
+    for batch in (1, 2, 7, 19, 64, 1000):
+        for L in (1, 2, 63, 64, 65, 1000, 2048, 4097, 16384, 65535, 65536, 1 << 20):
+            n, chunk = gqa.decode_plan(L, batch, sms)
+            assert chunk % 64 == 0 and chunk >= 64
+            assert n >= 1 and (n - 1) * chunk < L <= n * chunk
+            assert n <= (L + 63) // 64
+            if sms * 1 >= 8 * batch:
+                assert n * 8 * batch <= sms or n == 1
+            else:
+                assert n == 1
+    assert gqa.decode_plan(65536, 1, 152) == (19, 3456)
+
+
+def test_decode_plan_rejects_bad_arguments(lib):
+    with pytest.raises(ValueError):
+        gqa.decode_plan(0)
+    with pytest.raises(ValueError):
+        gqa.decode_plan(100, 0)
