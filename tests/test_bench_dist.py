@@ -54,3 +54,24 @@ def test_warmup_minimum():
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
+    """The reference arm (the fp64 oracle on the host cores) runs on CPU and
+    prints one JSON line with the contract's keys."""
+    import json
+    import bench
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3",
+                       "--ref-total", "2", "--ref-seconds", "0.5"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
