@@ -16,11 +16,13 @@
 //
 // One work item = one query head x 256 query rows, held as two 128-row Q
 // tiles (A and B) that share every K/V tile loaded into shared memory.
-// Roles (320 threads):
+// Roles (384 threads, three warpgroups):
 //   warps 0-3  softmax of tile A (thread r owns TMEM lane / query row r)
 //   warps 4-7  softmax of tile B
 //   warp  8    TMA producer: Q tiles, then K_j, V_j into a 4-slot ring
 //   warp  9    TMEM allocator and tcgen05.mma issuer (one thread)
+//   warps 10-11 idle (they complete the third warpgroup, whose registers
+//              setmaxnreg hands to the softmax warps)
 // TMEM (512 columns x 128 lanes, fp32):
 //   S_A [0,128)  S_B [128,256)  O_A [256,384)  O_B [384,512)
 //   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
@@ -45,7 +47,14 @@ constexpr int kHalfBytes = kTileBytes / 2;     // [128 rows][64 dims], 16 KB
 constexpr int kSoftmaxWarps = 4 * kTiles;
 constexpr int kWarpLoad = kSoftmaxWarps;       // 8
 constexpr int kWarpMma = kSoftmaxWarps + 1;    // 9
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+// 12 warps = three warpgroups: softmax A, softmax B, and producer + MMA +
+// two idle warps.  At launch every thread gets 168 registers (384 x 168 =
+// 64512); the third group lowers itself to 96 and the softmax groups raise
+// themselves to 200 (256 x 200 + 128 x 96 = 63488; per SMSP one warp of each
+// group: (200 + 200 + 96) x 32 = 15872 of 16384).
+constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 96;
 constexpr int kQBytes = kTiles * kTileBytes;
 constexpr int kRingBytes = kStages * kTileBytes;
 // q_full, q_empty, kv_full[4], kv_empty[4], s_full[2], p_full[2], o_full[2]
@@ -228,6 +237,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    if (warp >= kSoftmaxWarps) {
+        // producer / MMA warpgroup: give registers to the softmax groups
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther) : "memory");
     if (warp == kWarpLoad) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -354,7 +366,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
             }
         }
+    }  // warps 10 and 11 have no role
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
         // ------------------------------------------------------ softmax
         const int t = warp >> 2;             // 0 = tile A, 1 = tile B
         const int r = (warp & 3) * 32 + lane; // row inside the tile = TMEM lane
