@@ -28,6 +28,9 @@
 //   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
 // MMA issue order per KV tile j:  PV_A(j), S_A(j+1), PV_B(j), S_B(j+1):
 // while one tile's softmax runs, the tensor core works on the other's.
+// Row maxima of full tiles come out of the TMEM load itself (tcgen05.ld.red
+// .max, per thread over each 32 loaded columns); only a masked diagonal or
+// ragged tile takes its maximum in registers after masking.
 // O is rescaled only when a row maximum grows by more than 2^8 (the final
 // O / l uses the same stale maximum, so the result is unchanged).
 #include <cuda_bf16.h>
@@ -392,33 +395,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     break;
                 ++s_cnt;
                 tc_fence_after();
+                // S_t(j), with each row's maximum over every 32 columns
+                // reduced by the TMEM load itself
                 uint32_t sv[kBN];
+                float part_max[kBN / 32];
 #pragma unroll
                 for (int c = 0; c < kBN / 32; ++c)
-                    tmem_ld32(s_tm + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c));
+                    tmem_ld32_max(s_tm + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c),
+                                  part_max[c]);
                 tmem_wait_ld();
                 // keys kbase + c with c <= lim are visible to this row
                 const int kbase = j * kBN;
                 int lim = len - 1 - kbase;
                 if (causal && row - kbase < lim) lim = row - kbase;
+                float mx = fmaxf(fmax3(part_max[0], part_max[1], part_max[2]), part_max[3]);
                 if (lim < kBN - 1) {
+                    // diagonal or ragged last tile: mask, then take the row
+                    // maximum over the visible keys only (8 chains of 3-input max)
 #pragma unroll
                     for (int c = 0; c < kBN; ++c)
                         if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+                    float mx8[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        mx8[c] = fmaxf(__uint_as_float(sv[c]), __uint_as_float(sv[c + 8]));
+#pragma unroll
+                    for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            mx8[e] = fmax3(mx8[e], __uint_as_float(sv[c + e]),
+                                           __uint_as_float(sv[c + 8 + e]));
+                    mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
                 }
-                // row max: 8 independent chains of 3-input max, then a tree
-                float mx8[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    mx8[c] = fmaxf(__uint_as_float(sv[c]), __uint_as_float(sv[c + 8]));
-#pragma unroll
-                for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        mx8[e] = fmax3(mx8[e], __uint_as_float(sv[c + e]),
-                                       __uint_as_float(sv[c + 8 + e]));
-                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                       fmaxf(mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_run, mx * kScaleLog2);
                 float alpha = 1.f;
                 bool resc = false;
