@@ -26,8 +26,12 @@
 // TMEM (512 columns x 128 lanes, fp32):
 //   S_A [0,128)  S_B [128,256)  O_A [256,384)  O_B [384,512)
 //   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
-// MMA issue order per KV tile j:  PV_A(j), S_A(j+1), PV_B(j), S_B(j+1):
-// while one tile's softmax runs, the tensor core works on the other's.
+// MMA issue per KV tile j, two batches of 16 MMAs:  [PV_A(j), S_A(j+1)],
+// [PV_B(j), S_B(j+1)]: while one tile's softmax runs, the tensor core works
+// on the other's.  The issuing thread waits once per batch (on that tile's
+// P) and commits once per batch (S complete); the softmax warps check that
+// the batch's K/V tiles are resident before handing over P, and return ring
+// slots once a completed S_B implies every MMA that read them is done.
 // Row maxima of full tiles come out of the TMEM load itself (tcgen05.ld.red
 // .max, per thread over each 32 loaded columns); only a masked diagonal or
 // ragged tile takes its maximum in registers after masking.
@@ -52,12 +56,13 @@ constexpr int kWarpLoad = kSoftmaxWarps;       // 8
 constexpr int kWarpMma = kSoftmaxWarps + 1;    // 9
 // 12 warps = three warpgroups: softmax A, softmax B, and producer + MMA +
 // two idle warps.  At launch every thread gets 168 registers (384 x 168 =
-// 64512); the third group lowers itself to 96 and the softmax groups raise
-// themselves to 200 (256 x 200 + 128 x 96 = 63488; per SMSP one warp of each
-// group: (200 + 200 + 96) x 32 = 15872 of 16384).
+// 64512); the third group lowers itself to 104 and the softmax groups raise
+// themselves to 200 (256 x 200 + 128 x 104 = 64512, exactly what the third
+// group gives up; per SMSP one warp of each group: (200 + 200 + 104) x 32 =
+// 16128 of 16384).
 constexpr int kThreads = (kSoftmaxWarps + 4) * 32;
 constexpr int kRegsSoftmax = 200;
-constexpr int kRegsOther = 96;
+constexpr int kRegsOther = 104;
 constexpr int kQBytes = kTiles * kTileBytes;
 constexpr int kRingBytes = kStages * kTileBytes;
 // q_full, q_empty, kv_full[4], kv_empty[4], s_full[2], p_full[2], o_full[2]
@@ -287,14 +292,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------ MMA issuer
+        // Per KV step this thread polls only p_full(A) and p_full(B) and
+        // commits only s_full(A) and s_full(B): the softmax warps check that
+        // the step's K/V tiles are resident before they hand over P, and
+        // release ring slots once a completed S implies every MMA reading
+        // them has finished.  (A shared-memory poll right after a commit
+        // stalls this thread long enough to starve the shallow MMA queue.)
         if (lane == 0) {
-            int kv = 0;
+            int kv = 0;  // ring index of the next K/V tile (K_0 V_0 K_1 V_1 ...)
             int p_cnt[kTiles] = {0, 0};
             bool ok = true;
-            auto wait_kv = [&](int i) {
-                return lone_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err,
-                                 kErrWaitFull, abort);
-            };
+            auto ring = [&](int i) { return sRing + (i % kStages) * kTileBytes; };
             auto issue_s = [&](int t, uint32_t ktile) {
                 const uint32_t d = tmem + kBN * t;
                 const uint32_t qtile = sQ + t * kTileBytes;
@@ -310,7 +318,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     umma_ts(d, p + kk * 8, vdesc(vtile, kk), kIdescO, (!first || kk > 0));
-                umma_commit(bars.o_full(t));
+            };
+            auto wait_p = [&](int t) {
+                if (!lone_wait(bars.p_full(t), p_cnt[t] & 1, err, kErrWaitSoftmax, abort))
+                    return false;
+                ++p_cnt[t];
+                tc_fence_after();
+                return true;
             };
             for (int r = 0, n = 0; ok; ++r) {
                 const int idx = work.item(r, cta, G);
@@ -320,51 +334,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 const int nA = work.n_kv(it, 0), nB = work.n_kv(it, 1);
                 if (!(ok = lone_wait(bars.q_full(), n & 1, err, kErrWaitFull, abort))) break;
                 ++n;
-                tc_fence_after();
                 // K_0 -> S_A(0), S_B(0)
-                int kslot = kv % kStages;
-                if (!(ok = wait_kv(kv))) break;
+                if (!(ok = lone_wait(bars.kv_full(kv % kStages), (kv / kStages) & 1, err,
+                                     kErrWaitFull, abort)))
+                    break;
                 tc_fence_after();
-                issue_s(0, sRing + kslot * kTileBytes);
-                issue_s(1, sRing + kslot * kTileBytes);
-                umma_commit(bars.kv_empty(kslot));
+                issue_s(0, ring(kv));
+                issue_s(1, ring(kv));
                 ++kv;
                 if (nB == 1) umma_commit(bars.q_empty());
-                for (int j = 0; j < nB && ok; ++j) {
-                    const int vslot = kv % kStages;
-                    if (!(ok = wait_kv(kv))) break;
-                    ++kv;  // kv now indexes K_{j+1}
-                    const bool next = j + 1 < nB;
-                    kslot = kv % kStages;
-                    bool k_ready = false;
+                // step j: [PV_A(j), S_A(j+1)] then [PV_B(j), S_B(j+1)];
+                // kv indexes V_j, kv + 1 is K_{j+1}
+                for (int j = 0; j < nB; ++j) {
+                    const uint32_t vt = ring(kv), kt = ring(kv + 1);
                     if (j < nA) {
-                        if (!(ok = lone_wait(bars.p_full(0), p_cnt[0] & 1, err,
-                                             kErrWaitSoftmax, abort)))
-                            break;
-                        ++p_cnt[0];
-                        tc_fence_after();
-                        issue_pv(0, sRing + vslot * kTileBytes, j == 0);
-                        if (j + 1 < nA) {
-                            if (!(ok = wait_kv(kv))) break;
-                            k_ready = true;
-                            tc_fence_after();
-                            issue_s(0, sRing + kslot * kTileBytes);
-                        }
+                        if (!(ok = wait_p(0))) break;
+                        issue_pv(0, vt, j == 0);
+                        if (j + 1 < nA)
+                            issue_s(0, kt);
+                        else
+                            umma_commit(bars.o_full(0));
                     }
-                    if (!(ok = lone_wait(bars.p_full(1), p_cnt[1] & 1, err, kErrWaitSoftmax,
-                                         abort)))
-                        break;
-                    ++p_cnt[1];
-                    tc_fence_after();
-                    issue_pv(1, sRing + vslot * kTileBytes, j == 0);
-                    umma_commit(bars.kv_empty(vslot));
-                    if (next) {
-                        if (!k_ready && !(ok = wait_kv(kv))) break;
-                        tc_fence_after();
-                        issue_s(1, sRing + kslot * kTileBytes);
-                        umma_commit(bars.kv_empty(kslot));
-                        ++kv;
+                    if (!(ok = wait_p(1))) break;
+                    issue_pv(1, vt, j == 0);
+                    if (j + 1 < nB) {
+                        issue_s(1, kt);
+                        kv += 2;
                         if (j + 2 == nB) umma_commit(bars.q_empty());
+                    } else {
+                        umma_commit(bars.o_full(1));
+                        kv += 1;
                     }
                 }
             }
@@ -379,6 +378,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         const uint32_t s_tm = tmem + lane_field + kBN * t;
         const uint32_t o_tm = tmem + lane_field + 2 * kBN + kD * t;
         int s_cnt = 0, o_cnt = 0;
+        int kvb = 0;  // ring index of this item's K_0
+        // one thread returns K/V ring slots to the producer
+        const bool releaser = t == 1 && (warp & 3) == 0 && lane == 0;
         bool ok = true;
         for (int rr = 0; ok; ++rr) {
             const int idx = work.item(rr, cta, G);
@@ -388,6 +390,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             const int h = it.h, len = it.len;
             const int qt = 2 * it.b + t;
             const int n = work.n_kv(it, t);
+            const int nB = work.n_kv(it, 1);
             const int row = qt * kBM + r;  // row inside the sequence
             float m_run = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
@@ -395,6 +398,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     break;
                 ++s_cnt;
                 tc_fence_after();
+                if (releaser) {
+                    // S_B(j) complete: every MMA issued before it is too, so
+                    // K_j (read by S_A(j), S_B(j)) and V_{j-1} are free
+                    mbar_arrive(bars.kv_empty((kvb + 2 * j) % kStages));
+                    if (j > 0) mbar_arrive(bars.kv_empty((kvb + 2 * j - 1) % kStages));
+                }
+                // the MMA batch this tile's P releases reads V_j and, unless
+                // this is the tile's last step, K_{j+1}: both must be resident
+                // before P is handed over
+                {
+                    const int ev = kvb + 2 * j + 1;
+                    if (!(ok = warp_wait(bars.kv_full(ev % kStages), (ev / kStages) & 1, err,
+                                         kErrWaitFull, abort)))
+                        break;
+                    if (j + 1 < n &&
+                        !(ok = warp_wait(bars.kv_full((ev + 1) % kStages), ((ev + 1) / kStages) & 1,
+                                         err, kErrWaitFull, abort)))
+                        break;
+                }
                 // S_t(j), with each row's maximum over every 32 columns
                 // reduced by the TMEM load itself
                 uint32_t sv[kBN];
@@ -461,13 +483,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 tmem_st32(s_tm + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
                 tmem_wait_st();
                 if (j > 0) {
-                    // O of the previous KV tile must be complete before it is
-                    // rescaled (and before P_j is consumed, which keeps the
-                    // o_full phases matched one to one).
-                    if (!(ok = warp_wait(bars.o_full(t), o_cnt & 1, err, kErrWaitMma, abort)))
-                        break;
-                    ++o_cnt;
-                    tc_fence_after();
+                    // S_t(j) was issued after PV_t(j-1), so O is complete here
                     if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
                         for (int c = 0; c < kD / 32; ++c) {
@@ -491,6 +507,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             if (!(ok = warp_wait(bars.o_full(t), o_cnt & 1, err, kErrWaitMma, abort))) break;
             ++o_cnt;
             tc_fence_after();
+            if (releaser) mbar_arrive(bars.kv_empty((kvb + 2 * nB - 1) % kStages));  // V_last
+            kvb += 2 * nB;
             const float inv = 1.f / l;
             if (lse != nullptr && row < len)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
                 lse[size_t(h) * total + it.start + row] = (m_run + __log2f(l)) * kLn2;
