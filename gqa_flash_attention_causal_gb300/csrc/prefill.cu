@@ -21,7 +21,8 @@
 //   warps 4-7  softmax of tile B
 //   warp  8    TMA producer: Q tiles, then K_j, V_j into a 4-slot ring
 //   warp  9    TMEM allocator and tcgen05.mma issuer (one thread)
-//   warps 10-11 idle (they complete the third warpgroup, whose registers
+//   warp  10   ring bookkeeping: K/V residency checks and slot release
+//   warp  11   idle (completes the third warpgroup, whose registers
 //              setmaxnreg hands to the softmax warps)
 // TMEM (512 columns x 128 lanes, fp32):
 //   S_A [0,128)  S_B [128,256)  O_A [256,384)  O_B [384,512)
@@ -29,9 +30,9 @@
 // MMA issue per KV tile j, two batches of 16 MMAs:  [PV_A(j), S_A(j+1)],
 // [PV_B(j), S_B(j+1)]: while one tile's softmax runs, the tensor core works
 // on the other's.  The issuing thread waits once per batch (on that tile's
-// P) and commits once per batch (S complete); the softmax warps check that
-// the batch's K/V tiles are resident before handing over P, and return ring
-// slots once a completed S_B implies every MMA that read them is done.
+// P) and commits once per batch (S complete); the ring warp adds the
+// "K/V resident" condition to the same barrier and returns ring slots once a
+// completed S_B implies every MMA that read them is done.
 // Row maxima of full tiles come out of the TMEM load itself (tcgen05.ld.red
 // .max, per thread over each 32 loaded columns); only a masked diagonal or
 // ragged tile takes its maximum in registers after masking.
@@ -54,6 +55,7 @@ constexpr int kHalfBytes = kTileBytes / 2;     // [128 rows][64 dims], 16 KB
 constexpr int kSoftmaxWarps = 4 * kTiles;
 constexpr int kWarpLoad = kSoftmaxWarps;       // 8
 constexpr int kWarpMma = kSoftmaxWarps + 1;    // 9
+constexpr int kWarpRing = kSoftmaxWarps + 2;   // 10
 // 12 warps = three warpgroups: softmax A, softmax B, and producer + MMA +
 // two idle warps.  At launch every thread gets 168 registers (384 x 168 =
 // 64512); the third group lowers itself to 104 and the softmax groups raise
@@ -219,7 +221,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(bars.s_full(t), 1);
-            mbar_init(bars.p_full(t), 4);
+            mbar_init(bars.p_full(t), 4 + 1);  // the tile's softmax warps + ring warp
             mbar_init(bars.o_full(t), 1);
         }
         *abort = 0;
@@ -292,12 +294,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------ MMA issuer
-        // Per KV step this thread polls only p_full(A) and p_full(B) and
-        // commits only s_full(A) and s_full(B): the softmax warps check that
-        // the step's K/V tiles are resident before they hand over P, and
-        // release ring slots once a completed S implies every MMA reading
-        // them has finished.  (A shared-memory poll right after a commit
-        // stalls this thread long enough to starve the shallow MMA queue.)
+        // Per KV step this thread polls only p_full(A) and p_full(B) (which
+        // also carry "K/V resident", from the ring warp) and commits only
+        // s_full(A) and s_full(B).  A shared-memory poll right after a commit
+        // stalls this thread for about one MMA, and the tensor pipe queues
+        // only a few MMAs, so every extra poll between batches idles it.
         if (lane == 0) {
             int kv = 0;  // ring index of the next K/V tile (K_0 V_0 K_1 V_1 ...)
             int p_cnt[kTiles] = {0, 0};
@@ -368,7 +369,58 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 }
             }
         }
-    }  // warps 10 and 11 have no role
+    } else if (warp == kWarpRing) {
+        // ------------------------------------------------------ ring warp
+        // Keeps K/V bookkeeping off the softmax and MMA critical paths.  Per
+        // KV step j it waits until V_j and K_{j+1} are resident and adds the
+        // fifth arrival to p_full(A) / p_full(B), so a completed p_full means
+        // "P ready and operands resident".  Once p_full(B) of step j has
+        // completed, the softmax of B has seen S_B(j) complete, hence every
+        // MMA issued before it: K_j and V_{j-1} go back to the producer (the
+        // item's last V once its final PV has completed).
+        if (lane == 0) {
+            int kv = 0;  // ring index, as counted by the producer
+            int p_cnt[kTiles] = {0, 0};
+            int o_cnt = 0;
+            bool ok = true;
+            auto wait_ring = [&](int i) {
+                return lone_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err, kErrWaitFull,
+                                 abort);
+            };
+            for (int r = 0; ok; ++r) {
+                const int idx = work.item(r, cta, G);
+                if (idx >= work.n_items) break;
+                Item it;
+                if (!work.resolve(idx, it, err)) continue;
+                const int nA = work.n_kv(it, 0), nB = work.n_kv(it, 1);
+                const int k0 = kv;  // K_0; V_j = k0 + 2j + 1, K_j = k0 + 2j
+                for (int j = 0; j < nB && ok; ++j) {
+                    if (!(ok = wait_ring(k0 + 2 * j + 1))) break;
+                    if (j + 1 < nB && !(ok = wait_ring(k0 + 2 * j + 2))) break;
+                    if (j < nA) mbar_arrive(bars.p_full(0));
+                    mbar_arrive(bars.p_full(1));
+                    // one arrival per phase: wait for the phases to complete
+                    if (j < nA) {
+                        if (!(ok = lone_wait(bars.p_full(0), p_cnt[0] & 1, err, kErrWaitSoftmax,
+                                             abort)))
+                            break;
+                        ++p_cnt[0];
+                    }
+                    if (!(ok = lone_wait(bars.p_full(1), p_cnt[1] & 1, err, kErrWaitSoftmax,
+                                         abort)))
+                        break;
+                    ++p_cnt[1];
+                    mbar_arrive(bars.kv_empty((k0 + 2 * j) % kStages));                 // K_j
+                    if (j > 0) mbar_arrive(bars.kv_empty((k0 + 2 * j - 1) % kStages));  // V_{j-1}
+                }
+                if (!ok) break;
+                if (!(ok = lone_wait(bars.o_full(1), o_cnt & 1, err, kErrWaitMma, abort))) break;
+                ++o_cnt;
+                mbar_arrive(bars.kv_empty((k0 + 2 * nB - 1) % kStages));  // V_{nB-1}
+                kv = k0 + 2 * nB;
+            }
+        }
+    }  // warp 11 has no role
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
         // ------------------------------------------------------ softmax
@@ -378,9 +430,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         const uint32_t s_tm = tmem + lane_field + kBN * t;
         const uint32_t o_tm = tmem + lane_field + 2 * kBN + kD * t;
         int s_cnt = 0, o_cnt = 0;
-        int kvb = 0;  // ring index of this item's K_0
-        // one thread returns K/V ring slots to the producer
-        const bool releaser = t == 1 && (warp & 3) == 0 && lane == 0;
         bool ok = true;
         for (int rr = 0; ok; ++rr) {
             const int idx = work.item(rr, cta, G);
@@ -390,7 +439,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             const int h = it.h, len = it.len;
             const int qt = 2 * it.b + t;
             const int n = work.n_kv(it, t);
-            const int nB = work.n_kv(it, 1);
             const int row = qt * kBM + r;  // row inside the sequence
             float m_run = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
@@ -398,25 +446,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     break;
                 ++s_cnt;
                 tc_fence_after();
-                if (releaser) {
-                    // S_B(j) complete: every MMA issued before it is too, so
-                    // K_j (read by S_A(j), S_B(j)) and V_{j-1} are free
-                    mbar_arrive(bars.kv_empty((kvb + 2 * j) % kStages));
-                    if (j > 0) mbar_arrive(bars.kv_empty((kvb + 2 * j - 1) % kStages));
-                }
-                // the MMA batch this tile's P releases reads V_j and, unless
-                // this is the tile's last step, K_{j+1}: both must be resident
-                // before P is handed over
-                {
-                    const int ev = kvb + 2 * j + 1;
-                    if (!(ok = warp_wait(bars.kv_full(ev % kStages), (ev / kStages) & 1, err,
-                                         kErrWaitFull, abort)))
-                        break;
-                    if (j + 1 < n &&
-                        !(ok = warp_wait(bars.kv_full((ev + 1) % kStages), ((ev + 1) / kStages) & 1,
-                                         err, kErrWaitFull, abort)))
-                        break;
-                }
                 // S_t(j), with each row's maximum over every 32 columns
                 // reduced by the TMEM load itself
                 uint32_t sv[kBN];
@@ -507,8 +536,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             if (!(ok = warp_wait(bars.o_full(t), o_cnt & 1, err, kErrWaitMma, abort))) break;
             ++o_cnt;
             tc_fence_after();
-            if (releaser) mbar_arrive(bars.kv_empty((kvb + 2 * nB - 1) % kStages));  // V_last
-            kvb += 2 * nB;
             const float inv = 1.f / l;
             if (lse != nullptr && row < len)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
                 lse[size_t(h) * total + it.start + row] = (m_run + __log2f(l)) * kLn2;
