@@ -181,16 +181,29 @@ __device__ __forceinline__ bool lone_wait(uint32_t bar, uint32_t parity, unsigne
     return true;
 }
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-    // 16-dim K step kk of a [128 rows][128 dims] tile stored as two swizzled
-    // [128][64] halves: 32-byte steps inside a half, 8-row groups 1 KB apart.
-    return umma_desc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+// Shared-memory matrix descriptors, split into their two 32-bit words so the
+// issuing thread only adds a constant to the low word per MMA.  Low word:
+// start address >> 4 (bits 0-13) and leading byte offset >> 4 (bits 16-29);
+// high word: stride byte offset >> 4, descriptor version 1, 128-byte
+// swizzle (the fields of umma_desc_sw128).  Start addresses stay below
+// 256 KB, so adding (offset >> 4) to the low word never carries out of the
+// address field.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
-__device__ __forceinline__ uint64_t vdesc(uint32_t tile, int kk) {
-    // V as the MN-major B operand: 16-key step kk = 16 rows of 128 B; the two
-    // 64-dim halves are kHalfBytes apart (LBO), 8-key groups 1 KB apart (SBO).
-    return umma_desc_sw128(tile + kk * 2048, kHalfBytes, 1024);
+constexpr uint32_t kDescHi = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);  // SBO 1 KB
+__device__ __forceinline__ uint64_t desc(uint32_t lo) {
+    return (uint64_t(kDescHi) << 32) | lo;
 }
+// 16-dim K step kk of a K-major [128 rows][128 dims] tile stored as two
+// swizzled [128][64] halves (kHalfBytes apart), 32 bytes per step inside a
+// half, 8-row groups 1 KB apart (SBO): offset in 16-byte units.
+__host__ __device__ constexpr uint32_t kmajor_step(int kk) {
+    return uint32_t(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+}
+// V as the MN-major B operand: 16-key step kk = 16 rows of 128 B; the two
+// 64-dim halves are kHalfBytes apart (LBO), 8-key groups 1 KB apart (SBO).
+__host__ __device__ constexpr uint32_t v_step(int kk) { return uint32_t((kk * 2048) >> 4); }
 
 template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -303,22 +316,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             int kv = 0;  // ring index of the next K/V tile (K_0 V_0 K_1 V_1 ...)
             int p_cnt[kTiles] = {0, 0};
             bool ok = true;
-            auto ring = [&](int i) { return sRing + (i % kStages) * kTileBytes; };
-            auto issue_s = [&](int t, uint32_t ktile) {
+            // descriptor low words: Q tiles A and B, ring slot 0 as a K-major
+            // (LBO 16 B) and as an MN-major V (LBO = kHalfBytes) operand
+            const uint32_t q_lo[kTiles] = {desc_lo(sQ, 16), desc_lo(sQ + kTileBytes, 16)};
+            const uint32_t k_lo0 = desc_lo(sRing, 16), v_lo0 = desc_lo(sRing, kHalfBytes);
+            constexpr uint32_t kSlotStep = kTileBytes >> 4;
+            auto issue_s = [&](int t, int slot) {
                 const uint32_t d = tmem + kBN * t;
-                const uint32_t qtile = sQ + t * kTileBytes;
+                const uint32_t k_lo = k_lo0 + uint32_t(slot) * kSlotStep;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    umma_ss(d, kmajor_desc(qtile, kk), kmajor_desc(ktile, kk), kIdescS,
-                            kk > 0);
+                    umma_ss(d, desc(q_lo[t] + kmajor_step(kk)), desc(k_lo + kmajor_step(kk)),
+                            kIdescS, kk > 0);
                 umma_commit(bars.s_full(t));
             };
-            auto issue_pv = [&](int t, uint32_t vtile, bool first) {
+            auto issue_pv = [&](int t, int slot, bool first) {
                 const uint32_t d = tmem + 2 * kBN + kD * t;
                 const uint32_t p = tmem + kBN * t;
+                const uint32_t v_lo = v_lo0 + uint32_t(slot) * kSlotStep;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma_ts(d, p + kk * 8, vdesc(vtile, kk), kIdescO, (!first || kk > 0));
+                    umma_ts(d, p + kk * 8, desc(v_lo + v_step(kk)), kIdescO, (!first || kk > 0));
             };
             auto wait_p = [&](int t) {
                 if (!lone_wait(bars.p_full(t), p_cnt[t] & 1, err, kErrWaitSoftmax, abort))
@@ -340,14 +358,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                                      kErrWaitFull, abort)))
                     break;
                 tc_fence_after();
-                issue_s(0, ring(kv));
-                issue_s(1, ring(kv));
+                issue_s(0, kv % kStages);
+                issue_s(1, kv % kStages);
                 ++kv;
                 if (nB == 1) umma_commit(bars.q_empty());
                 // step j: [PV_A(j), S_A(j+1)] then [PV_B(j), S_B(j+1)];
                 // kv indexes V_j, kv + 1 is K_{j+1}
                 for (int j = 0; j < nB; ++j) {
-                    const uint32_t vt = ring(kv), kt = ring(kv + 1);
+                    const int vt = kv % kStages, kt = (kv + 1) % kStages;
                     if (j < nA) {
                         if (!(ok = wait_p(0))) break;
                         issue_pv(0, vt, j == 0);
