@@ -78,3 +78,31 @@ def test_prefill_deterministic():
     b = gqa.prefill(dq, dk, dv)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("ramp", ["growing", "shrinking"])
+def test_prefill_running_max_paths(causal, ramp):
+    """Keys whose magnitude grows along the sequence push every row's maximum
+    up by far more than the lazy-rescale threshold (2^8) at every KV tile, so
+    O and l are rescaled tile after tile; shrinking keys keep the maximum in
+    the first tile, so later tiles contribute weights near 2^-large.  Both
+    must match the oracle over full rows.  The scores are large (q x4, keys
+    up to x11), so attention is peaked and |out| approaches max|v|: the
+    large-magnitude rule applies (both bounds times max|v|)."""
+    from gqa_flash_attention_causal_gb300.inputs import normal_bf16
+    S = 1024
+    q = normal_bf16((1, S, 32, 128), 11, 4.0)
+    k = normal_bf16((1, S, 8, 128), 12)
+    v = normal_bf16((1, S, 8, 128), 13)
+    pos = torch.arange(S, dtype=torch.float32)
+    gain = 1.0 + 10.0 * pos / S if ramp == "growing" else 11.0 - 10.0 * pos / S
+    k = (k.float() * gain[None, :, None, None]).to(torch.bfloat16)
+    out = poisoned((1, S, 32, 128))
+    gqa.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, out=out)
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    mx, mean = assert_close(out, oracle.prefill(q, k, v, causal=causal)[None],
+                            scale=tolerance_scale(v, True), what=f"{ramp} keys, causal={causal}")
+    # the bf16 rounding of a peaked output dominates: still well inside 1 % of max|v|
+    assert mx <= 0.01 * tolerance_scale(v, True)
