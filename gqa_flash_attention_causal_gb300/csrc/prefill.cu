@@ -32,7 +32,10 @@
 // on the other's.  The issuing thread waits once per batch (on that tile's
 // P) and commits once per batch (S complete); the ring warp adds the
 // "K/V resident" condition to the same barrier and returns ring slots once a
-// completed S_B implies every MMA that read them is done.
+// completed S_B implies every MMA that read them is done.  O's completion is
+// signalled once per item (for the epilogue): S_t(j) follows PV_t(j-1) in
+// the in-order tensor pipe, so a completed S_t(j) already implies that O is
+// complete for the softmax's rescale.
 // Row maxima of full tiles come out of the TMEM load itself (tcgen05.ld.red
 // .max, per thread over each 32 loaded columns); only a masked diagonal or
 // ragged tile takes its maximum in registers after masking.
@@ -57,7 +60,7 @@ constexpr int kWarpLoad = kSoftmaxWarps;       // 8
 constexpr int kWarpMma = kSoftmaxWarps + 1;    // 9
 constexpr int kWarpRing = kSoftmaxWarps + 2;   // 10
 // 12 warps = three warpgroups: softmax A, softmax B, and producer + MMA +
-// two idle warps.  At launch every thread gets 168 registers (384 x 168 =
+// ring + one idle warp.  At launch every thread gets 168 registers (384 x 168 =
 // 64512); the third group lowers itself to 104 and the softmax groups raise
 // themselves to 200 (256 x 200 + 128 x 104 = 64512, exactly what the third
 // group gives up; per SMSP one warp of each group: (200 + 200 + 104) x 32 =
