@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -81,13 +82,22 @@ KERNEL_SOURCES = {"prefill": ("prefill.cu", "ptx.cuh", "internal.h"),
                   "decode": ("decode.cu", "ptx.cuh", "internal.h")}
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace collapsed, so that a
+    comment-only edit does not count as a kernel change."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """Hash of the source files that define `kernel` (prefill or decode)."""
+    """Hash of the code (comments ignored) of the source files that define
+    `kernel` (prefill or decode)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_flash_attention_causal_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
