@@ -99,3 +99,10 @@ def test_decode_deterministic():
     b = gqa.decode(dq, dk, dv)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_decode_large_cache():
+    """L = 2^20: each cache spans 2 GiB, so chunk offsets past 2^31 bytes
+    must be computed in 64 bits."""
+    (q, kc, vc), out = run(1 << 20)
+    assert_close(out, oracle.decode(q, kc, vc), what="L=2^20")

@@ -106,3 +106,20 @@ def test_prefill_running_max_paths(causal, ramp):
                             scale=tolerance_scale(v, True), what=f"{ramp} keys, causal={causal}")
     # the bf16 rounding of a peaked output dominates: still well inside 1 % of max|v|
     assert mx <= 0.01 * tolerance_scale(v, True)
+
+
+def test_prefill_causal_large_sampled():
+    """S = 2^18: q and out span 2 GiB each, so every byte offset past 2^31
+    must be computed in 64 bits; sampled rows include both ends, tile and
+    item boundaries near the end of the sequence."""
+    S = 1 << 18
+    q, k, v = prefill_inputs(S)
+    out = poisoned((1, S, 32, 128))
+    gqa.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, out=out)
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    rows = [0, 127, 128, 255, 256, S // 2, S - 257, S - 256, S - 129, S - 128, S - 2, S - 1]
+    want = oracle.prefill_rows(q, k, v, rows, causal=True)
+    assert_close(out[0, rows], want, what=f"causal S={S} sampled")
+    # every row was written (rows past the last item would stay NaN)
+    assert bool(torch.isfinite(out[0, ::997].float()).all())
