@@ -33,6 +33,8 @@ SIGNATURES = {
     "gqa_attn_decode_lse": (_I, [_P, _P, _P, _P, _P, _I, _P]),
     "gqa_attn_prefill_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gqa_attn_decode_batched": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
+    "gqa_attn_prefill_heads": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "gqa_attn_decode_heads": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_workspace_bytes": (_S, [_I]),
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
@@ -212,6 +214,74 @@ def decode_batched(q, kcache, vcache, seqlens=None, out=None, stream=None,
         q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(),
         lse.data_ptr() if lse is not None else None,
         seqlens.data_ptr() if seqlens is not None else None, B, Lmax, _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def prefill_heads(q, k, v, cu_seqlens=None, max_seqlen=None, causal: bool = True, out=None,
+                  stream=None, return_lse: bool = False):
+    """Prefill for any head layout (query heads a multiple of KV heads):
+    q [1,S,Hq,128] with k/v [1,S,Hkv,128], or packed q [total,Hq,128] with
+    k/v [total,Hkv,128] and ``cu_seqlens`` (int32 CUDA tensor of batch+1
+    offsets) plus ``max_seqlen``.  Returns out shaped like q (and lse
+    [Hq,total] fp32 with ``return_lse``)."""
+    import torch
+    if q.dim() == 4:
+        if cu_seqlens is not None:
+            raise ValueError("4-D tensors are one sequence; pass packed 3-D tensors with cu_seqlens")
+        total, hq, hkv = q.shape[1], q.shape[2], k.shape[2]
+        _expect(q, (1, total, hq, HEAD_DIM), "q")
+        _expect(k, (1, total, hkv, HEAD_DIM), "k")
+        _expect(v, (1, total, hkv, HEAD_DIM), "v")
+        batch, max_seqlen = 1, total
+    else:
+        total, hq, hkv = q.shape[0], q.shape[1], k.shape[1]
+        _expect(q, (total, hq, HEAD_DIM), "q")
+        _expect(k, (total, hkv, HEAD_DIM), "k")
+        _expect(v, (total, hkv, HEAD_DIM), "v")
+        if cu_seqlens is None:
+            batch, max_seqlen = 1, total
+        else:
+            if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+                raise TypeError("cu_seqlens must be a 1-D int32 CUDA tensor")
+            if max_seqlen is None:
+                raise ValueError("max_seqlen is required with cu_seqlens")
+            batch = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, tuple(q.shape), "out")
+    lse = torch.empty((hq, total), dtype=torch.float32, device=q.device) if return_lse else None
+    _check("gqa_attn_prefill_heads", lib().gqa_attn_prefill_heads(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None,
+        cu_seqlens.data_ptr() if cu_seqlens is not None else None, batch, int(max_seqlen),
+        total, hq, hkv, 1 if causal else 0, _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def decode_heads(q, kcache, vcache, seqlens=None, out=None, stream=None,
+                 return_lse: bool = False):
+    """Decode for any head layout with at most 8 query heads per KV head:
+    q [B,Hq,128] against caches [B,Lmax,Hkv,128] bf16; sequence b attends to
+    its first seqlens[b] rows (int32 CUDA tensor [B]; None = all Lmax).
+    Returns out [B,Hq,128] (and lse [B,Hq] fp32)."""
+    import torch
+    B, hq = q.shape[0], q.shape[1]
+    Lmax, hkv = kcache.shape[1], kcache.shape[2]
+    _expect(q, (B, hq, HEAD_DIM), "q")
+    _expect(kcache, (B, Lmax, hkv, HEAD_DIM), "kcache")
+    _expect(vcache, (B, Lmax, hkv, HEAD_DIM), "vcache")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or not seqlens.is_cuda
+                                or tuple(seqlens.shape) != (B,)):
+        raise TypeError("seqlens must be an int32 CUDA tensor of shape [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, (B, hq, HEAD_DIM), "out")
+    lse = torch.empty((B, hq), dtype=torch.float32, device=q.device) if return_lse else None
+    _check("gqa_attn_decode_heads", lib().gqa_attn_decode_heads(
+        q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None,
+        seqlens.data_ptr() if seqlens is not None else None, B, Lmax, hq, hkv,
+        _stream(stream)))
     return (out, lse) if return_lse else out
 
 

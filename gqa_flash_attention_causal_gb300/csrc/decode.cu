@@ -34,9 +34,11 @@ constexpr int kTileBytes = 2 * kHalfBytes;       // K (or V) tile, 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;      // K + V, 32 KB
 constexpr int kThreads = (kWarps + 1) * 32;      // + one TMA producer warp
 constexpr int kCtasPerSm = 1;
-constexpr int kCmbFloats = kWarps * kGroup * kD; // cross-warp merge buffer
+// query heads per KV head the kernel handles: the warp MMA's 8 N columns
+constexpr int kMaxGroup = 8;
+constexpr int kCmbFloats = kWarps * kMaxGroup * kD; // cross-warp merge buffer
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + size_t(kStages) * kStageBytes +
-                              size_t(kCmbFloats) * 4 + 2 * kWarps * kGroup * 4 +
+                              size_t(kCmbFloats) * 4 + 2 * kWarps * kMaxGroup * 4 +
                               2 * kStages * 8;
 
 static_assert(kStageKeys == kDecodeBoxRows, "tensor-map box must match a stage");
@@ -44,19 +46,23 @@ static_assert(kStageKeys == kDecodeBoxRows, "tensor-map box must match a stage")
 // log2(e) / sqrt(128): scores are kept in the base-2 domain.
 constexpr float kScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
 
+// kFixedGroup > 0: the query heads per KV head are a compile-time constant
+// (the 32/8 layout); 0: they come from `group_arg` (1..kMaxGroup).
+template <int kFixedGroup>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
                     const __nv_bfloat16 *__restrict__ q, const int *__restrict__ seqlens,
-                    int Lmax, int chunk, float *__restrict__ part_o,
+                    int Lmax, int chunk, int hq, int group_arg, float *__restrict__ part_o,
                     float *__restrict__ part_lse, unsigned *err) {
+    const int group = kFixedGroup > 0 ? kFixedGroup : group_arg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *cmb_o = reinterpret_cast<float *>(smem + kStages * kStageBytes);
     float *cmb_m = cmb_o + kCmbFloats;
-    float *cmb_l = cmb_m + kWarps * kGroup;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cmb_l + kWarps * kGroup);
+    float *cmb_l = cmb_m + kWarps * kMaxGroup;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cmb_l + kWarps * kMaxGroup);
     const uint32_t tiles = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
 
@@ -66,9 +72,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     // this CTA's chunk of sequence `seq`, whose cache holds rows
     // seq*Lmax .. seq*Lmax + L - 1 of the tensor maps
     const int row0 = seq * Lmax;
-    q += size_t(seq) * kHq * kD;
-    part_o += size_t(seq) * n_split * kHq * kD;
-    part_lse += size_t(seq) * n_split * kHq;
+    q += size_t(seq) * hq * kD;
+    part_o += size_t(seq) * n_split * hq * kD;
+    part_lse += size_t(seq) * n_split * hq;
 
     // Let the combine kernel (a programmatic dependent) get scheduled now; it
     // still waits for this whole grid to finish before reading its results.
@@ -135,9 +141,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     uint32_t qf[8][2];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        if (gi < kGroup) {
+        if (gi < group) {
             const uint32_t *qh = reinterpret_cast<const uint32_t *>(
-                q + (g * kGroup + gi) * kD + 16 * kk + 2 * ti);
+                q + (g * group + gi) * kD + 16 * kk + 2 * ti);
             qf[kk][0] = __ldg(qh);
             qf[kk][1] = __ldg(qh + 4);
         } else {
@@ -213,11 +219,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 
     if (n_iter == 0) {  // no keys here: a partial that carries no weight
         const int t = threadIdx.x;
-        const int n = t >> 5, d0 = (t & 31) * 4;
-        const int hq = g * kGroup + n;
-        *reinterpret_cast<float4 *>(part_o + (size_t(split) * kHq + hq) * kD + d0) =
-            make_float4(0.f, 0.f, 0.f, 0.f);
-        if (d0 == 0) part_lse[split * kHq + hq] = -INFINITY;
+        const int d0 = (t & 31) * 4;
+        for (int n = t >> 5; n < group; n += kWarps) {
+            const int h = g * group + n;
+            *reinterpret_cast<float4 *>(part_o + (size_t(split) * hq + h) * kD + d0) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+            if (d0 == 0) part_lse[split * hq + h] = -INFINITY;
+        }
         return;
     }
 
@@ -227,10 +235,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    if (ti < 2) {
+    if (2 * ti < group) {  // lane owns query heads 2ti and 2ti+1 of the group
         const int h0 = 2 * ti, h1 = 2 * ti + 1;
-        float *w0 = cmb_o + (warp * kGroup + h0) * kD;
-        float *w1 = cmb_o + (warp * kGroup + h1) * kD;
+        float *w0 = cmb_o + (warp * kMaxGroup + h0) * kD;
+        float *w1 = cmb_o + (warp * kMaxGroup + h1) * kD;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const int d = 16 * mt + gi;
@@ -240,36 +248,39 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             w1[d + 8] = o[mt][3];
         }
         if (gi == 0) {
-            cmb_m[warp * kGroup + h0] = m0;
-            cmb_m[warp * kGroup + h1] = m1;
-            cmb_l[warp * kGroup + h0] = l0;
-            cmb_l[warp * kGroup + h1] = l1;
+            cmb_m[warp * kMaxGroup + h0] = m0;
+            cmb_m[warp * kMaxGroup + h1] = m1;
+            cmb_l[warp * kMaxGroup + h0] = l0;
+            cmb_l[warp * kMaxGroup + h1] = l1;
         }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
 
-    const int t = threadIdx.x;            // 0..127
-    const int n = t >> 5, d0 = (t & 31) * 4;
-    float M = -INFINITY;
+    const int t = threadIdx.x;            // 0..127: query head n, dims d0..d0+3
+    const int d0 = (t & 31) * 4;
+    for (int n = t >> 5; n < group; n += kWarps) {
+        float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmb_m[w * kGroup + n]);
-    float den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmb_m[w * kMaxGroup + n]);
+        float den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const float mw = cmb_m[w * kGroup + n];
-        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-        den += f * cmb_l[w * kGroup + n];
-        const float4 v = *reinterpret_cast<const float4 *>(cmb_o + (w * kGroup + n) * kD + d0);
-        acc[0] += f * v.x;
-        acc[1] += f * v.y;
-        acc[2] += f * v.z;
-        acc[3] += f * v.w;
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = cmb_m[w * kMaxGroup + n];
+            const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+            den += f * cmb_l[w * kMaxGroup + n];
+            const float4 v =
+                *reinterpret_cast<const float4 *>(cmb_o + (w * kMaxGroup + n) * kD + d0);
+            acc[0] += f * v.x;
+            acc[1] += f * v.y;
+            acc[2] += f * v.z;
+            acc[3] += f * v.w;
+        }
+        const float inv = 1.f / den;
+        const int h = g * group + n;
+        *reinterpret_cast<float4 *>(part_o + (size_t(split) * hq + h) * kD + d0) =
+            make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        if (d0 == 0) part_lse[split * hq + h] = M + __log2f(den);
     }
-    const float inv = 1.f / den;
-    const int hq = g * kGroup + n;
-    *reinterpret_cast<float4 *>(part_o + (size_t(split) * kHq + hq) * kD + d0) =
-        make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    if (d0 == 0) part_lse[split * kHq + hq] = M + __log2f(den);
 }
 
 // Merge the chunk results of every query head: with per-chunk normalised
@@ -282,7 +293,7 @@ constexpr int kCmbUnroll = 4;
 
 __global__ void __launch_bounds__(kCmbWarps * 32)
 decode_combine_kernel(const float *__restrict__ part_o,
-                      const float *__restrict__ part_lse, int n_split,
+                      const float *__restrict__ part_lse, int n_split, int hq,
                       __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
                       const int *__restrict__ seqlens, int Lmax) {
     // Launched as a programmatic dependent of the split kernel: wait until
@@ -296,10 +307,10 @@ decode_combine_kernel(const float *__restrict__ part_o,
         const int L = __ldg(seqlens + seq);
         if (L < 1 || L > Lmax) return;  // flagged by the split kernel; out untouched
     }
-    part_o += size_t(seq) * n_split * kHq * kD;
-    part_lse += size_t(seq) * n_split * kHq;
-    out += size_t(seq) * kHq * kD;
-    if (lse != nullptr) lse += size_t(seq) * kHq;
+    part_o += size_t(seq) * n_split * hq * kD;
+    part_lse += size_t(seq) * n_split * hq;
+    out += size_t(seq) * hq * kD;
+    if (lse != nullptr) lse += size_t(seq) * hq;
     const int d0 = lane * 4;
     float m = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -310,9 +321,9 @@ decode_combine_kernel(const float *__restrict__ part_o,
         for (int u = 0; u < kCmbUnroll; ++u) {  // issue every load first
             const int s = s0 + u * kCmbWarps;
             if (s < n_split) {
-                l[u] = __ldcg(part_lse + s * kHq + h);
+                l[u] = __ldcg(part_lse + s * hq + h);
                 o[u] = __ldcg(reinterpret_cast<const float4 *>(
-                    part_o + (size_t(s) * kHq + h) * kD + d0));
+                    part_o + (size_t(s) * hq + h) * kD + d0));
             }
         }
 #pragma unroll
@@ -362,10 +373,10 @@ decode_combine_kernel(const float *__restrict__ part_o,
 
 }  // namespace
 
-DecodePlan decode_plan(int Lmax, int batch, int num_sms) {
+DecodePlan decode_plan(int Lmax, int batch, int num_sms, int hq, int hkv) {
     const int max_split = (Lmax + kStageKeys - 1) / kStageKeys;
     // one wave of (split, KV head, sequence) CTAs
-    int n = num_sms * kCtasPerSm / (kHkv * batch);
+    int n = int(num_sms * kCtasPerSm / (static_cast<long long>(hkv) * batch));
     if (n < 1) n = 1;
     if (n > max_split) n = max_split;
     int chunk = (Lmax + n - 1) / n;
@@ -374,13 +385,15 @@ DecodePlan decode_plan(int Lmax, int batch, int num_sms) {
     p.chunk = chunk;
     p.n_split = (Lmax + chunk - 1) / chunk;
     p.batch = batch;
+    p.hq = hq;
+    p.hkv = hkv;
     return p;
 }
 
 size_t decode_workspace_bytes(const DecodePlan &p) {
     const size_t parts = size_t(p.n_split) * p.batch;
-    const size_t o = parts * kHq * kD * sizeof(float);
-    const size_t lse = parts * kHq * sizeof(float);
+    const size_t o = parts * p.hq * kD * sizeof(float);
+    const size_t lse = parts * p.hq * sizeof(float);
     return o + ((lse + 255) / 256) * 256;
 }
 
@@ -393,13 +406,18 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel,
+        e = cudaFuncSetAttribute(decode_split_kernel<kGroup>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_split_kernel<0>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(kSmemBytes));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
+    const int group = plan.hq / plan.hkv;
     float *part_o = static_cast<float *>(workspace);
-    float *part_lse = part_o + size_t(plan.n_split) * plan.batch * kHq * kD;
+    float *part_lse = part_o + size_t(plan.n_split) * plan.batch * plan.hq * kD;
 
     // Both kernels are programmatic dependents of their predecessor on the
     // stream: their launch and set-up overlap it, and each waits
@@ -408,23 +426,24 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.n_split, kHkv, plan.batch);
+    cfg.gridDim = dim3(plan.n_split, plan.hkv, plan.batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_split_kernel, kmap, vmap,
-                           static_cast<const __nv_bfloat16 *>(q), seqlens, Lmax, plan.chunk,
-                           part_o, part_lse, err);
+    e = cudaLaunchKernelEx(&cfg, group == kGroup ? decode_split_kernel<kGroup>
+                                                 : decode_split_kernel<0>,
+                           kmap, vmap, static_cast<const __nv_bfloat16 *>(q), seqlens, Lmax,
+                           plan.chunk, plan.hq, group, part_o, part_lse, err);
     if (e != cudaSuccess) return e;
 
-    cfg.gridDim = dim3(kHq, plan.batch);
+    cfg.gridDim = dim3(plan.hq, plan.batch);
     cfg.blockDim = dim3(kCmbWarps * 32);
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel,
                               static_cast<const float *>(part_o),
-                              static_cast<const float *>(part_lse), plan.n_split,
+                              static_cast<const float *>(part_lse), plan.n_split, plan.hq,
                               static_cast<__nv_bfloat16 *>(out), lse, seqlens, Lmax);
 }
 

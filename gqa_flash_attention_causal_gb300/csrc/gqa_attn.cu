@@ -32,6 +32,7 @@ constexpr int kMaxPrefillLen = 1 << 20;
 constexpr int kMaxPrefillTotal = 1 << 24;  // rows of a packed batch
 constexpr int kMaxDecodeLen = 1 << 26;
 constexpr long long kMaxDecodeRows = 1ll << 30;  // batch x cache rows
+constexpr int kMaxHeads = 256;                  // query heads of the *_heads entries
 
 struct DeviceState {
     bool probed = false;
@@ -193,8 +194,8 @@ gqa_status run_decode(const void *q, const void *kc, const void *vc, void *out, 
                       unsigned *err, cudaStream_t stream) {
     CUtensorMap kmap, vmap;
     const int rows = Lmax * plan.batch;
-    gqa_status st = encode_bshd(&kmap, kc, rows, kHkv, gqa::kDecodeBoxRows);
-    if (st == GQA_OK) st = encode_bshd(&vmap, vc, rows, kHkv, gqa::kDecodeBoxRows);
+    gqa_status st = encode_bshd(&kmap, kc, rows, plan.hkv, gqa::kDecodeBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, vc, rows, plan.hkv, gqa::kDecodeBoxRows);
     if (st != GQA_OK) return st;
     return from_cuda(gqa::launch_decode(kmap, vmap, q, out, lse, seqlens, Lmax, plan, ws, err,
                                         stream));
@@ -232,7 +233,7 @@ extern "C" {
 // null: one sequence of `total` rows).
 static gqa_status prefill_impl(const void *q, const void *k, const void *v, void *out,
                                float *lse, const int *cu, int B, int max_len, int total,
-                               int causal, cudaStream_t stream) {
+                               int causal, int hq, int hkv, cudaStream_t stream) {
     if (!q || !k || !v || !out) return GQA_ERR_NULL;
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
         return GQA_ERR_ALIGN;
@@ -241,8 +242,9 @@ static gqa_status prefill_impl(const void *q, const void *k, const void *v, void
     if (B < 1 || max_len < 1 || max_len > kMaxPrefillLen || total < 1 ||
         total > kMaxPrefillTotal)
         return GQA_ERR_SHAPE;
+    if (hkv < 1 || hq < hkv || hq > kMaxHeads || hq % hkv != 0) return GQA_ERR_SHAPE;
     const long long blocks = ((max_len + 127) / 128 + 1) / 2;
-    if (blocks * B * kHq > 0x7fffffffLL) return GQA_ERR_SHAPE;
+    if (blocks * B * hq > 0x7fffffffLL) return GQA_ERR_SHAPE;
     DeviceState *dev = nullptr;
     gqa_status st = current_device(&dev);
     if (st != GQA_OK) return st;
@@ -253,23 +255,24 @@ static gqa_status prefill_impl(const void *q, const void *k, const void *v, void
     if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
     if (cu && (st = check_device_ptr(cu)) != GQA_OK) return st;
     CUtensorMap qmap, kmap, vmap;
-    st = encode_bshd(&qmap, q, total, kHq, gqa::kPrefillBoxRows);
-    if (st == GQA_OK) st = encode_bshd(&kmap, k, total, kHkv, gqa::kPrefillBoxRows);
-    if (st == GQA_OK) st = encode_bshd(&vmap, v, total, kHkv, gqa::kPrefillBoxRows);
+    st = encode_bshd(&qmap, q, total, hq, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&kmap, k, total, hkv, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, v, total, hkv, gqa::kPrefillBoxRows);
     if (st != GQA_OK) return st;
     return from_cuda(gqa::launch_prefill(qmap, kmap, vmap, out, lse, cu, B, max_len, total,
-                                         causal ? 1 : 0, dev->num_sms, dev->err, stream));
+                                         causal ? 1 : 0, hq, hkv, dev->num_sms, dev->err,
+                                         stream));
 }
 
 gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *out, int S,
                             int causal, cudaStream_t stream) {
-    return prefill_impl(q, k, v, out, nullptr, nullptr, 1, S, S, causal, stream);
+    return prefill_impl(q, k, v, out, nullptr, nullptr, 1, S, S, causal, kHq, kHkv, stream);
 }
 
 gqa_status gqa_attn_prefill_lse(const void *q, const void *k, const void *v, void *out,
                                 float *lse, int S, int causal, cudaStream_t stream) {
     if (!lse) return GQA_ERR_NULL;
-    return prefill_impl(q, k, v, out, lse, nullptr, 1, S, S, causal, stream);
+    return prefill_impl(q, k, v, out, lse, nullptr, 1, S, S, causal, kHq, kHkv, stream);
 }
 
 gqa_status gqa_attn_prefill_varlen(const void *q, const void *k, const void *v, void *out,
@@ -277,8 +280,18 @@ gqa_status gqa_attn_prefill_varlen(const void *q, const void *k, const void *v, 
                                    int max_seqlen, int total, int causal,
                                    cudaStream_t stream) {
     if (!cu_seqlens) return GQA_ERR_NULL;
+    return prefill_impl(q, k, v, out, lse, cu_seqlens, batch, max_seqlen, total, causal, kHq,
+                        kHkv, stream);
+}
+
+gqa_status gqa_attn_prefill_heads(const void *q, const void *k, const void *v, void *out,
+                                  float *lse, const int *cu_seqlens, int batch, int max_seqlen,
+                                  int total, int num_q_heads, int num_kv_heads, int causal,
+                                  cudaStream_t stream) {
+    if (!cu_seqlens && batch != 1) return GQA_ERR_SHAPE;
+    if (!cu_seqlens && max_seqlen != total) return GQA_ERR_SHAPE;
     return prefill_impl(q, k, v, out, lse, cu_seqlens, batch, max_seqlen, total, causal,
-                        stream);
+                        num_q_heads, num_kv_heads, stream);
 }
 
 size_t gqa_attn_decode_workspace_bytes(int L) {
@@ -345,9 +358,9 @@ gqa_status gqa_attn_decode_lse(const void *q, const void *kcache, const void *vc
     return decode_impl(q, kcache, vcache, out, lse, L, stream);
 }
 
-gqa_status gqa_attn_decode_batched(const void *q, const void *kcache, const void *vcache,
-                                   void *out, float *lse, const int *seqlens, int batch,
-                                   int max_len, cudaStream_t stream) {
+static gqa_status decode_batched_impl(const void *q, const void *kcache, const void *vcache,
+                                      void *out, float *lse, const int *seqlens, int batch,
+                                      int max_len, int hq, int hkv, cudaStream_t stream) {
     if (!q || !kcache || !vcache || !out) return GQA_ERR_NULL;
     if (misaligned(q) || misaligned(kcache) || misaligned(vcache) || misaligned(out))
         return GQA_ERR_ALIGN;
@@ -356,6 +369,9 @@ gqa_status gqa_attn_decode_batched(const void *q, const void *kcache, const void
         return GQA_ERR_ALIGN;
     if (batch < 1 || max_len < 1 || max_len > kMaxDecodeLen ||
         (long long)batch * max_len > kMaxDecodeRows)
+        return GQA_ERR_SHAPE;
+    if (hkv < 1 || hq < hkv || hq > kMaxHeads || hq % hkv != 0 ||
+        hq / hkv > gqa::kDecodeMaxGroup)
         return GQA_ERR_SHAPE;
     DeviceState *dev = nullptr;
     gqa_status st = current_device(&dev);
@@ -366,12 +382,27 @@ gqa_status gqa_attn_decode_batched(const void *q, const void *kcache, const void
     }
     if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
     if (seqlens && (st = check_device_ptr(seqlens)) != GQA_OK) return st;
-    const gqa::DecodePlan plan = gqa::decode_plan(max_len, batch, dev->num_sms);
+    const gqa::DecodePlan plan = gqa::decode_plan(max_len, batch, dev->num_sms, hq, hkv);
     void *ws = nullptr;
     st = library_workspace(dev, gqa::decode_workspace_bytes(plan), &ws);
     if (st != GQA_OK) return st;
     return run_decode(q, kcache, vcache, out, lse, seqlens, max_len, plan, ws, dev->err,
                       stream);
+}
+
+gqa_status gqa_attn_decode_batched(const void *q, const void *kcache, const void *vcache,
+                                   void *out, float *lse, const int *seqlens, int batch,
+                                   int max_len, cudaStream_t stream) {
+    return decode_batched_impl(q, kcache, vcache, out, lse, seqlens, batch, max_len, kHq, kHkv,
+                               stream);
+}
+
+gqa_status gqa_attn_decode_heads(const void *q, const void *kcache, const void *vcache,
+                                 void *out, float *lse, const int *seqlens, int batch,
+                                 int max_len, int num_q_heads, int num_kv_heads,
+                                 cudaStream_t stream) {
+    return decode_batched_impl(q, kcache, vcache, out, lse, seqlens, batch, max_len,
+                               num_q_heads, num_kv_heads, stream);
 }
 
 gqa_status gqa_attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,

@@ -108,11 +108,12 @@ struct Item {
 template <bool kVarlen>
 struct Work {
     const int *cu;
-    int B, total, n_blocks, n_items, causal;
-    __device__ Work(const int *cu_, int B_, int max_len, int total_, int causal_)
-        : cu(cu_), B(B_), total(total_), causal(causal_) {
+    int B, total, n_blocks, n_items, causal, hq, group;
+    __device__ Work(const int *cu_, int B_, int max_len, int total_, int causal_, int hq_,
+                    int group_)
+        : cu(cu_), B(B_), total(total_), causal(causal_), hq(hq_), group(group_) {
         n_blocks = ((max_len + kBM - 1) / kBM + 1) / 2;
-        n_items = n_blocks * B * kHq;
+        n_items = n_blocks * B * hq;
     }
     // Item of round `r` for CTA `c` (snake order over the grid).
     __device__ int item(int r, int c, int G) const {
@@ -121,11 +122,11 @@ struct Work {
     // false: nothing to do for this item (past its sequence, or a malformed
     // cu array, which also sets kErrBadSeqlens)
     __device__ bool resolve(int idx, Item &it, unsigned *err) const {
-        const int per_block = B * kHq;
+        const int per_block = B * hq;
         it.b = causal ? n_blocks - 1 - idx / per_block : idx / per_block;
         const int rem = idx % per_block;
-        const int seq = rem / kHq;
-        it.h = rem % kHq;
+        const int seq = rem / hq;
+        it.h = rem % hq;
         if (kVarlen) {
             it.start = __ldg(cu + seq);
             it.len = __ldg(cu + seq + 1) - it.start;
@@ -214,7 +215,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, __nv_bfloat16 *__restrict__ out,
                float *__restrict__ lse, const int *__restrict__ cu_seqlens, int B,
-               int max_len, int total, int causal, unsigned *err) {
+               int max_len, int total, int causal, int hq, int group, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -225,7 +226,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const Bars bars{smem_u32(bar_mem)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Work<kVarlen> work(cu_seqlens, B, max_len, total, causal);
+    const Work<kVarlen> work(cu_seqlens, B, max_len, total, causal, hq, group);
     const int G = gridDim.x, cta = blockIdx.x;
 
     if (threadIdx.x == 0) {
@@ -278,7 +279,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                 if (idx >= work.n_items) break;
                 Item it;
                 if (!work.resolve(idx, it, err)) continue;
-                const int h = it.h, g = h / kGroup;
+                const int h = it.h, g = h / work.group;
                 if (n > 0 && !(ok = lone_wait(bars.q_empty(), (n - 1) & 1, err,
                                               kErrWaitEmpty, abort)))
                     break;
@@ -560,7 +561,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             const float inv = 1.f / l;
             if (lse != nullptr && row < len)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
                 lse[size_t(h) * total + it.start + row] = (m_run + __log2f(l)) * kLn2;
-            __nv_bfloat16 *dst = out + (size_t(it.start + row) * kHq + h) * kD;
+            __nv_bfloat16 *dst = out + (size_t(it.start + row) * work.hq + h) * kD;
 #pragma unroll
             for (int c = 0; c < kD / 32; ++c) {
                 uint32_t ov[32];
@@ -593,7 +594,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 template <bool kVarlen>
 cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                    void *out, float *lse, const int *cu_seqlens, int B, int max_len, int total,
-                   int causal, int num_sms, unsigned *err, cudaStream_t stream) {
+                   int causal, int hq, int hkv, int num_sms, unsigned *err,
+                   cudaStream_t stream) {
     static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -604,7 +606,7 @@ cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUten
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const long long n_items = ((max_len + kBM - 1) / kBM + 1) / 2 * (long long)B * kHq;
+    const long long n_items = ((max_len + kBM - 1) / kBM + 1) / 2 * (long long)B * hq;
     const int grid = n_items < num_sms ? int(n_items) : num_sms;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -618,7 +620,7 @@ cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUten
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_kernel<kVarlen>, qmap, kmap, vmap,
                               static_cast<__nv_bfloat16 *>(out), lse, cu_seqlens, B, max_len,
-                              total, causal, err);
+                              total, causal, hq, hq / hkv, err);
 }
 
 }  // namespace
@@ -626,13 +628,13 @@ cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUten
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, void *out, float *lse,
                            const int *cu_seqlens, int B, int max_len, int total, int causal,
-                           int num_sms, unsigned *err, cudaStream_t stream) {
+                           int hq, int hkv, int num_sms, unsigned *err, cudaStream_t stream) {
     // one sequence: the instantiation without per-sequence offsets
     if (cu_seqlens == nullptr)
-        return launch<false>(qmap, kmap, vmap, out, lse, nullptr, 1, total, total, causal,
-                             num_sms, err, stream);
-    return launch<true>(qmap, kmap, vmap, out, lse, cu_seqlens, B, max_len, total, causal,
-                        num_sms, err, stream);
+        return launch<false>(qmap, kmap, vmap, out, lse, nullptr, 1, total, total, causal, hq,
+                             hkv, num_sms, err, stream);
+    return launch<true>(qmap, kmap, vmap, out, lse, cu_seqlens, B, max_len, total, causal, hq,
+                        hkv, num_sms, err, stream);
 }
 
 }  // namespace gqa

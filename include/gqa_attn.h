@@ -97,6 +97,25 @@ gqa_status gqa_attn_prefill_varlen(const void *q, const void *k, const void *v,
                                    cudaStream_t stream);
 
 /*
+ * Prefill for other head layouts (the pages' model is the 32 / 8 case; the
+ * pages have no counterpart for other counts): num_q_heads query heads share
+ * num_kv_heads KV heads, query head h reading KV head
+ * h / (num_q_heads / num_kv_heads); head dim 128.  Otherwise exactly
+ * gqa_attn_prefill_varlen with the head counts in place of 32 and 8:
+ *     q, out [total][num_q_heads][128],  k, v [total][num_kv_heads][128]
+ * bf16, lse (may be NULL) [num_q_heads][total] fp32.  cu_seqlens may be NULL
+ * for a single sequence (then batch = 1 and max_seqlen = total).
+ * 1 <= num_kv_heads <= num_q_heads <= 256, num_q_heads a multiple of
+ * num_kv_heads (num_kv_heads = num_q_heads: multi-head attention;
+ * num_kv_heads = 1: multi-query attention); otherwise GQA_ERR_SHAPE.
+ */
+gqa_status gqa_attn_prefill_heads(const void *q, const void *k, const void *v,
+                                  void *out, float *lse, const int *cu_seqlens,
+                                  int batch, int max_seqlen, int total,
+                                  int num_q_heads, int num_kv_heads, int causal,
+                                  cudaStream_t stream);
+
+/*
  * Decode: one query token against a KV cache of length L (every cached
  * position is attended).  q, out: [1][1][32][128] bf16; kcache, vcache:
  * [1][L][8][128] bf16; 1 <= L <= 2^26.
@@ -134,6 +153,22 @@ gqa_status gqa_attn_decode_batched(const void *q, const void *kcache,
                                    const void *vcache, void *out, float *lse,
                                    const int *seqlens, int batch, int max_len,
                                    cudaStream_t stream);
+
+/*
+ * Decode for other head layouts (the pages have no counterpart): exactly
+ * gqa_attn_decode_batched with num_q_heads / num_kv_heads in place of 32 / 8:
+ *     q, out [batch][num_q_heads][128],  caches [batch][max_len][num_kv_heads][128]
+ * bf16, lse (may be NULL) [batch][num_q_heads] fp32.  The query heads of a
+ * KV head are computed together from one pass over its cache, which holds
+ * at most 8 of them: 1 <= num_kv_heads <= num_q_heads <= 256,
+ * num_q_heads a multiple of num_kv_heads and num_q_heads / num_kv_heads
+ * <= 8; otherwise GQA_ERR_SHAPE.
+ */
+gqa_status gqa_attn_decode_heads(const void *q, const void *kcache,
+                                 const void *vcache, void *out, float *lse,
+                                 const int *seqlens, int batch, int max_len,
+                                 int num_q_heads, int num_kv_heads,
+                                 cudaStream_t stream);
 
 /* Bytes of device workspace gqa_attn_decode_ws needs for length L (0 if L
  * is out of range). */

@@ -62,6 +62,22 @@ def test_bad_lengths_rejected_without_device(lib):
     assert lib.gqa_attn_decode_num_splits(-3) == 0
 
 
+def test_bad_head_counts_rejected_without_device(lib):
+    p = ctypes.c_void_p(4096)
+    # (query heads, KV heads): not a multiple, zero, more KV than query heads, > 256
+    for hq, hkv in ((32, 5), (32, 0), (8, 16), (512, 8), (0, 0), (-8, -4)):
+        assert lib.gqa_attn_prefill_heads(p, p, p, p, None, None, 1, 64, 64, hq, hkv, 1,
+                                          None) == 3, (hq, hkv)
+        assert lib.gqa_attn_decode_heads(p, p, p, p, None, None, 1, 64, hq, hkv,
+                                         None) == 3, (hq, hkv)
+    # decode holds at most 8 query heads per KV head
+    for hq, hkv in ((32, 2), (16, 1), (72, 8)):
+        assert lib.gqa_attn_decode_heads(p, p, p, p, None, None, 1, 64, hq, hkv, None) == 3
+    # a single sequence (no cu_seqlens) must have batch 1 and max_seqlen == total
+    assert lib.gqa_attn_prefill_heads(p, p, p, p, None, None, 2, 64, 128, 32, 8, 1, None) == 3
+    assert lib.gqa_attn_prefill_heads(p, p, p, p, None, None, 1, 64, 65, 32, 8, 1, None) == 3
+
+
 def test_launch_counts(lib):
     assert lib.gqa_attn_launches_per_call(0) == 1
     assert lib.gqa_attn_launches_per_call(1) == 2
