@@ -85,15 +85,39 @@ def _check(fn: str, code: int):
         raise GqaError(fn, code)
 
 
+_torch_refs = None
+
+
+def _refs():
+    """(torch, torch.bfloat16, raw current-stream getter, current-device
+    getter), looked up once: every call goes through here."""
+    global _torch_refs
+    if _torch_refs is None:
+        import torch
+        _torch_refs = (torch, torch.bfloat16,
+                       getattr(torch._C, "_cuda_getCurrentRawStream", None),
+                       getattr(torch._C, "_cuda_getDevice", None))
+    return _torch_refs
+
+
 def _stream(stream):
-    import torch
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    """cudaStream_t (as an int) of `stream`, default torch's current stream
+    on the current device."""
+    if stream is not None:
+        return stream.cuda_stream
+    torch, _, raw_stream, cur_dev = _refs()
+    if raw_stream is not None and cur_dev is not None:
+        return raw_stream(cur_dev())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _expect(t, shape, name):
-    import torch
+    torch, bf16 = _refs()[:2]
+    try:  # the common case in one expression; the checks below name the failure
+        if t.dtype is bf16 and t.is_cuda and t.shape == shape and t.is_contiguous():
+            return
+    except AttributeError:
+        pass
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != torch.bfloat16:
