@@ -396,18 +396,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         // Keeps K/V bookkeeping off the softmax and MMA critical paths.  Per
         // KV step j it waits until V_j and K_{j+1} are resident and adds the
         // fifth arrival to p_full(A) / p_full(B), so a completed p_full means
-        // "P ready and operands resident".  Once p_full(B) of step j has
-        // completed, the softmax of B has seen S_B(j) complete, hence every
-        // MMA issued before it: K_j and V_{j-1} go back to the producer (the
-        // item's last V once its final PV has completed).
+        // "P ready and operands resident".  Then, as soon as S_B(j) has
+        // completed (and with it every MMA issued before it, all reads of K_j
+        // and V_{j-1}), those two slots go back to the producer: a softmax
+        // earlier than waiting for P_B(j), which keeps the refill's ~1100-cycle
+        // TMA latency off the MMA's wait for P_A(j+1).  The item's last V goes
+        // back once its final PV has completed.
         if (lane == 0) {
             int kv = 0;  // ring index, as counted by the producer
             int p_cnt[kTiles] = {0, 0};
-            int o_cnt = 0;
+            int o_cnt = 0, s_cnt = 0;
             bool ok = true;
             auto wait_ring = [&](int i) {
                 return lone_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err, kErrWaitFull,
                                  abort);
+            };
+            // Until S_B of this step has completed.  Either barrier proves it:
+            // s_full(B) completing that phase, or p_full(B) completing this
+            // step's phase (its softmax has seen S_B).  s_full(B) can only be
+            // two phases ahead (its parity then reads "not complete" again)
+            // once p_full(B) has completed, and p_full(B) cannot run ahead of
+            // this warp, whose arrival each of its phases needs.
+            auto wait_sb = [&](int pb) {
+                const long long t0 = clock64();
+                while (!mbar_test_wait(bars.s_full(1), s_cnt & 1) &&
+                       !mbar_test_wait(bars.p_full(1), pb & 1)) {
+                    if (*abort || clock64() - t0 > kWaitLimitCycles) {
+                        atomicOr(err, kErrWaitMma);
+                        *abort = 1;
+                        return false;
+                    }
+                    __nanosleep(32);
+                }
+                return true;
             };
             for (int r = 0; ok; ++r) {
                 const int idx = work.item(r, cta, G);
@@ -421,6 +442,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     if (j + 1 < nB && !(ok = wait_ring(k0 + 2 * j + 2))) break;
                     if (j < nA) mbar_arrive(bars.p_full(0));
                     mbar_arrive(bars.p_full(1));
+                    if (!(ok = wait_sb(p_cnt[1]))) break;
+                    ++s_cnt;
+                    mbar_arrive(bars.kv_empty((k0 + 2 * j) % kStages));                 // K_j
+                    if (j > 0) mbar_arrive(bars.kv_empty((k0 + 2 * j - 1) % kStages));  // V_{j-1}
                     // one arrival per phase: wait for the phases to complete
                     if (j < nA) {
                         if (!(ok = lone_wait(bars.p_full(0), p_cnt[0] & 1, err, kErrWaitSoftmax,
@@ -432,8 +457,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                                          abort)))
                         break;
                     ++p_cnt[1];
-                    mbar_arrive(bars.kv_empty((k0 + 2 * j) % kStages));                 // K_j
-                    if (j > 0) mbar_arrive(bars.kv_empty((k0 + 2 * j - 1) % kStages));  // V_{j-1}
                 }
                 if (!ok) break;
                 if (!(ok = lone_wait(bars.o_full(1), o_cnt & 1, err, kErrWaitMma, abort))) break;
