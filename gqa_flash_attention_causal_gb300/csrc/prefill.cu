@@ -72,7 +72,11 @@ constexpr int kQBytes = kTiles * kTileBytes;
 constexpr int kRingBytes = kStages * kTileBytes;
 // q_full, q_empty, kv_full[4], kv_empty[4], s_full[2], p_full[2], o_full[2]
 constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles;
-constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16;
+// epilogue staging: per softmax warp, 32 rows x 64 columns of bf16 output
+constexpr int kStageWarpBytes = 32 * 64 * 2;
+constexpr int kStageBytes = kSoftmaxWarps * kStageWarpBytes;
+constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kStageBytes + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kBM == kPrefillBoxRows && kBN == kPrefillBoxRows, "tensor-map box");
@@ -221,7 +225,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sRing = sQ + kQBytes;
-    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + kQBytes + kRingBytes);
+    const uint32_t sStage = sRing + kRingBytes;
+    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + kQBytes + kRingBytes + kStageBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mem + kNumBars);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const Bars bars{smem_u32(bar_mem)};
@@ -584,23 +589,41 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             const float inv = 1.f / l;
             if (lse != nullptr && row < len)  // ln sum_j exp(s_j) = ln2 * (m + log2 l)
                 lse[size_t(h) * total + it.start + row] = (m_run + __log2f(l)) * kLn2;
-            __nv_bfloat16 *dst = out + (size_t(it.start + row) * work.hq + h) * kD;
+            // Each thread holds one row; stored directly, every warp store
+            // would touch 32 rows.  So each half (64 columns) goes through
+            // this warp's staging buffer (16-byte chunk k of row r at chunk
+            // k ^ (r & 7): conflict-free both ways) and leaves as 128-byte row
+            // segments, four rows per warp store.
+            const uint32_t stage = sStage + uint32_t(warp) * kStageWarpBytes;
+            const int row0 = qt * kBM + (warp & 3) * 32;  // this warp's first row
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(o_tm + 32 * c, ov);
-                tmem_wait_ld();
-                uint32_t pk[16];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv,
-                                      __uint_as_float(ov[2 * e + 1]) * inv);
-                if (row < len) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(o_tm + 64 * half + 32 * c, ov);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    for (int e = 0; e < 16; ++e)
+                        pk[16 * c + e] = pack_bf16(__uint_as_float(ov[2 * e]) * inv,
+                                                   __uint_as_float(ov[2 * e + 1]) * inv);
                 }
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(stage + lane * 128 + ((k ^ (lane & 7)) << 4), pk[4 * k],
+                                 pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int sr = 4 * i + (lane >> 3), k = lane & 7;
+                    const uint4 v = ld_shared_v4(stage + sr * 128 + ((k ^ (sr & 7)) << 4));
+                    if (row0 + sr < len)
+                        *reinterpret_cast<uint4 *>(
+                            out + (size_t(it.start + row0 + sr) * work.hq + h) * kD + 64 * half +
+                            8 * k) = v;
+                }
+                __syncwarp();
             }
             tc_fence_before();
         }
