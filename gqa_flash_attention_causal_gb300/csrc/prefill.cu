@@ -41,6 +41,8 @@
 // ragged tile takes its maximum in registers after masking.
 // O is rescaled only when a row maximum grows by more than 2^8 (the final
 // O / l uses the same stale maximum, so the result is unchanged).
+// The epilogue (softmax warps) stages each warp's 32 output rows in shared
+// memory and writes them as 128-byte row segments.
 #include <cuda_bf16.h>
 
 #include "internal.h"
