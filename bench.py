@@ -525,6 +525,26 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def sweep_time(fn, calls=1, burn_in=50, rounds=8):
+    """Per-call GPU time of `fn` (which makes `calls` calls): at least
+    `burn_in` calls first, then `rounds` timed rounds (CUDA events on the
+    current stream).  Returns (median, p05, p95) over rounds, ms per call."""
+    import numpy as np
+    import torch
+    for _ in range(max(1, -(-burn_in // calls))):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(rounds):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / calls)
+    return (float(np.median(ts)), float(np.percentile(ts, 5)), float(np.percentile(ts, 95)))
+
+
 def sweep_batch(kind, shape, dev, peaks, src):
     """Throughput and parity of a packed prefill batch or a batched decode."""
     import numpy as np
@@ -533,18 +553,12 @@ def sweep_batch(kind, shape, dev, peaks, src):
     import oracle
     from gqa_flash_attention_causal_gb300.inputs import normal_bf16
 
-    def med_time(fn, n=5):
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(n):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+    def med_time(fn):
+        t = sweep_time(fn)
+        stats.update({"ms_p05": t[1], "ms_p95": t[2]})
+        return t[0]
+
+    stats = {}
 
     if kind == "varlen":
         lens = list(shape)
@@ -585,6 +599,7 @@ def sweep_batch(kind, shape, dev, peaks, src):
                 "frac_of_measured_hbm": tput / peaks["hbm_gbs"],
                 "frac_of_8tbs": tput / NORTH_STAR_HBM_GBS,
                 "note": "eager calls; the batch's caches exceed L2"}
+    line.update(stats)
     line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
                  "parity_ok": bool(err.max() <= 2e-2 and err.mean() <= 2e-3), "peaks": src})
     if gqa.device_error() != 0:
@@ -607,19 +622,6 @@ def run_sweep(args):
     gqa.lib()
     rng = np.random.default_rng(0)
 
-    def med_time(fn, n=5):
-        fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(n):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
     cases = [("prefill", S, False) for S in (512, 2048, 4096, 8192, 16384, 32768)]
     cases += [("prefill", 4096, True)]
     cases += [("prefill_full", S, False) for S in (4096, 16384)]
@@ -638,7 +640,7 @@ def run_sweep(args):
             dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
             out = torch.empty_like(dq)
             call = lambda: gqa.prefill(dq, dk, dv, causal=causal, out=out)  # noqa: E731
-            ms_eager = med_time(call)
+            ms_eager = sweep_time(call)[0]
             # GPU time per call: a CUDA graph of back-to-back calls (at small
             # S a single eager call is dominated by the host-side launch path)
             reps = max(1, min(200, int(2.0 / max(ms_eager, 1e-3))))
@@ -651,7 +653,7 @@ def run_sweep(args):
                     for _ in range(reps):
                         call()
             torch.cuda.current_stream().wait_stream(side)
-            ms = med_time(g.replay) / reps
+            ms, p05, p95 = sweep_time(g.replay, calls=reps)
             call()
             rows = sorted({0, 1, n - 1, n // 2} | set(rng.integers(0, n, 30).tolist()))
             t0 = time.perf_counter()
@@ -665,8 +667,8 @@ def run_sweep(args):
             else:
                 oracle_ms = 1e3 * t_or * n / len(rows)
                 tput = 2.0 * prefill_flops(n) / (ms * 1e-3) / 1e12  # 4*S^2*H*D
-            line = {"workload": kind, "S": n, "stress": stress, "ms": ms, "ms_eager_call": ms_eager,
-                    "graph_reps": reps, "tflops": tput,
+            line = {"workload": kind, "S": n, "stress": stress, "ms": ms, "ms_p05": p05,
+                    "ms_p95": p95, "ms_eager_call": ms_eager, "graph_reps": reps, "tflops": tput,
                     "frac_of_burst": tput / peaks["bf16_tflops"],
                     "frac_of_sustained": tput / peaks["bf16_tflops_sustained"]}
         else:
@@ -686,14 +688,15 @@ def run_sweep(args):
                     for c in caches:
                         gqa.decode(dq, *c, out=out, workspace=ws)
             torch.cuda.current_stream().wait_stream(side)
-            ms = med_time(g.replay) / copies
+            ms, p05, p95 = sweep_time(g.replay, calls=copies)
             gqa.decode(dq, *caches[0], out=out, workspace=ws)
             t0 = time.perf_counter()
             want = oracle.decode(q, kc, vc)
             oracle_ms = 1e3 * (time.perf_counter() - t0)
             got = out.double().cpu().numpy().reshape(want.shape)
             tput = decode_bytes(n) / (ms * 1e-3) / 1e9
-            line = {"workload": "decode", "L": n, "stress": stress, "ms": ms, "gbs": tput,
+            line = {"workload": "decode", "L": n, "stress": stress, "ms": ms, "ms_p05": p05,
+                    "ms_p95": p95, "gbs": tput,
                     "frac_of_measured_hbm": tput / peaks["hbm_gbs"],
                     "frac_of_8tbs": tput / NORTH_STAR_HBM_GBS, "cache_copies": copies}
             del caches
