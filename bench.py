@@ -545,6 +545,77 @@ def sweep_time(fn, calls=1, burn_in=50, rounds=8):
     return (float(np.median(ts)), float(np.percentile(ts, 5)), float(np.percentile(ts, 95)))
 
 
+def _graph(calls):
+    """A CUDA graph replaying `calls` (callables) once each, captured on a
+    side stream after one eager round."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for c in calls:
+            c()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for c in calls:
+                c()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    return g
+
+
+def sweep_heads(kind, hq, hkv, n, dev, peaks, src):
+    """Throughput and parity of the runtime head-count entries
+    (gqa_attn_prefill_heads / gqa_attn_decode_heads) for one layout."""
+    import numpy as np
+    import torch
+    import gqa_flash_attention_causal_gb300 as gqa
+    import oracle
+    from gqa_flash_attention_causal_gb300.inputs import normal_bf16
+    if kind == "prefill":
+        q = normal_bf16((1, n, hq, D), 1)
+        k = normal_bf16((1, n, hkv, D), 2)
+        v = normal_bf16((1, n, hkv, D), 3)
+        dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+        out = torch.empty_like(dq)
+        call = lambda: gqa.prefill_heads(dq, dk, dv, out=out)  # noqa: E731
+        ms_eager = sweep_time(call)[0]
+        reps = max(1, min(200, int(2.0 / max(ms_eager, 1e-3))))
+        ms, p05, p95 = sweep_time(_graph([call] * reps).replay, calls=reps)
+        call()
+        torch.cuda.synchronize()
+        rows = sorted({0, 1, n // 2, n - 1})
+        err = np.abs(out[0, rows].double().cpu().numpy() - oracle.prefill_rows(q, k, v, rows))
+        tput = 2.0 * n * n * hq * D / (ms * 1e-3) / 1e12
+        line = {"workload": "prefill_heads", "hq": hq, "hkv": hkv, "S": n, "ms": ms,
+                "ms_p05": p05, "ms_p95": p95, "tflops": tput,
+                "frac_of_burst": tput / peaks["bf16_tflops"]}
+    else:
+        q = normal_bf16((1, hq, D), 1)
+        kc = normal_bf16((1, n, hkv, D), 2)
+        vc = normal_bf16((1, n, hkv, D), 3)
+        dq = q.to(dev)
+        nbytes = 2 * n * hkv * D * 2 + 2 * hq * D * 2
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        copies = max(1, -(-2 * l2 // (nbytes - 2 * hq * D * 2)) + 1)
+        caches = [(kc.to(dev), vc.to(dev)) for _ in range(copies)]
+        out = torch.empty_like(dq)
+        calls = [lambda c=c: gqa.decode_heads(dq, c[0], c[1], out=out) for c in caches]
+        ms, p05, p95 = sweep_time(_graph(calls).replay, calls=copies)
+        calls[0]()
+        torch.cuda.synchronize()
+        err = np.abs(out[0].double().cpu().numpy() - oracle.decode(q[0], kc[0], vc[0]))
+        tput = nbytes / (ms * 1e-3) / 1e9
+        line = {"workload": "decode_heads", "hq": hq, "hkv": hkv, "L": n, "ms": ms,
+                "ms_p05": p05, "ms_p95": p95, "gbs": tput,
+                "frac_of_measured_hbm": tput / peaks["hbm_gbs"], "cache_copies": copies}
+        del caches
+    line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
+                 "parity_ok": bool(err.max() <= 2e-2 and err.mean() <= 2e-3), "peaks": src})
+    if gqa.device_error() != 0:
+        raise RuntimeError("device-side wait timed out")
+    return line
+
+
 def sweep_batch(kind, shape, dev, peaks, src):
     """Throughput and parity of a packed prefill batch or a batched decode."""
     import numpy as np
@@ -630,7 +701,12 @@ def run_sweep(args):
     cases += [("varlen", (4096,) * 8, False), ("varlen", (8192, 4096, 2048, 1024, 512, 256), False)]
     cases += [("batched", (8, 8192), False), ("batched", (32, 4096), False),
               ("batched", (128, 2048), False)]
+    cases += [("heads", ("prefill", 64, 8, 8192), False), ("heads", ("prefill", 32, 32, 8192), False),
+              ("heads", ("decode", 64, 8, 32768), False), ("heads", ("decode", 32, 32, 16384), False)]
     for kind, n, stress in cases:
+        if kind == "heads":
+            print(json.dumps(sweep_heads(*n, dev, peaks, src)), flush=True)
+            continue
         if kind in ("varlen", "batched"):
             print(json.dumps(sweep_batch(kind, n, dev, peaks, src)), flush=True)
             continue
