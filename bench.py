@@ -120,7 +120,9 @@ class ClockSampler:
     reasons; `mark_start`/`mark_stop` bracket the timed region and only the
     samples taken inside it are summarised."""
 
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    # power.draw is a one-second average on this part; the timed region is
+    # shorter, so the instantaneous reading is the one that means something
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
