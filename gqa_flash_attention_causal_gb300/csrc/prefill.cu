@@ -77,7 +77,12 @@ constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles;
 // epilogue staging: per softmax warp, 32 rows x 64 columns of bf16 output
 constexpr int kStageWarpBytes = 32 * 64 * 2;
 constexpr int kStageBytes = kSoftmaxWarps * kStageWarpBytes;
-constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kStageBytes + kNumBars * 8 + 16;
+// packed batches up to this many sequences use the compact item order (Work)
+constexpr int kCompactBatch = 64;
+constexpr int kTabBytes = kCompactBatch * 8;
+constexpr int kCursorBytes = 16 * (kSoftmaxWarps + 4);  // one slot per warp
+constexpr size_t kSmemBytes =
+    1024 + kQBytes + kRingBytes + kStageBytes + kTabBytes + kCursorBytes + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 
@@ -111,15 +116,45 @@ struct Item {
     int b, h, start, len, T;
 };
 
-template <bool kVarlen>
+// 256-row blocks of a sequence of `len` rows.
+__device__ __forceinline__ int blocks_of(int len) { return ((len + kBM - 1) / kBM + 1) / 2; }
+
+// Items (block b, sequence, head), dealt longest first: block-major with b
+// descending (causal) or ascending.  A packed batch of at most
+// kCompactBatch sequences comes with a shared-memory table {start, len} per
+// sequence and skips the blocks past each sequence's end, so the empty items
+// a mixed-length batch would otherwise leave in some CTAs' share are gone
+// (schedule balance on lengths 8192..256: 0.83 -> 0.99); its order is b
+// descending, then sequence, then head.  Each role warp walks its items in
+// increasing index order, which its cursor relies on: (cb, cbase, ck) = block
+// cb holds items cbase .. cbase + hq*ck - 1, kept in a per-warp shared-memory
+// slot after the table (every lane of a warp computes the same values).
+template <bool kVarlen, bool kCompact>
 struct Work {
     const int *cu;
+    uint32_t tab;  // compact order: shared address of {start, len} per sequence, else 0
     int B, total, n_blocks, n_items, causal, hq, group;
-    __device__ Work(const int *cu_, int B_, int max_len, int total_, int causal_, int hq_,
-                    int group_)
-        : cu(cu_), B(B_), total(total_), causal(causal_), hq(hq_), group(group_) {
+    __device__ Work(const int *cu_, uint32_t tab_, int B_, int max_len, int total_,
+                    int causal_, int hq_, int group_)
+        : cu(cu_), tab(tab_), B(B_), total(total_), causal(causal_), hq(hq_), group(group_) {
         n_blocks = ((max_len + kBM - 1) / kBM + 1) / 2;
-        n_items = n_blocks * B * hq;
+        if (kCompact) {
+            int blocks = 0;
+            for (int s = 0; s < B; ++s) blocks += blocks_of(len_of(s));
+            n_items = blocks * hq;
+            const uint32_t c = cursor();
+            st_shared_v4(c, uint32_t(n_blocks), 0u, 0u, 0u);
+        } else {
+            n_items = n_blocks * B * hq;
+        }
+    }
+    __device__ int len_of(int s) const { return ld_shared_s32(tab + 8 * s + 4); }
+    __device__ uint32_t cursor() const { return tab + kTabBytes + 16 * (threadIdx.x >> 5); }
+    // sequences with more than b blocks
+    __device__ int count(int b) const {
+        int c = 0;
+        for (int s = 0; s < B; ++s) c += blocks_of(len_of(s)) > b;
+        return c;
     }
     // Item of round `r` for CTA `c` (snake order over the grid).
     __device__ int item(int r, int c, int G) const {
@@ -127,7 +162,36 @@ struct Work {
     }
     // false: nothing to do for this item (past its sequence, or a malformed
     // cu array, which also sets kErrBadSeqlens)
+    // Compact order (see above).  The lanes of a warp may interleave their
+    // reads and writes of the cursor slot in any order: all compute the same
+    // state for the same index, and a lane that reads the already advanced
+    // state finds its item in it directly.
+    __device__ bool resolve_compact(int idx, Item &it) const {
+        const uint32_t c = cursor();
+        const uint4 cur = ld_shared_v4(c);
+        int cb = int(cur.x), cbase = int(cur.y), ck = int(cur.z);
+        while (idx >= cbase + hq * ck) {
+            cbase += hq * ck;
+            if (--cb < 0) return false;
+            ck = count(cb);
+        }
+        st_shared_v4(c, uint32_t(cb), uint32_t(cbase), uint32_t(ck), 0u);
+        const int off = idx - cbase, rank = off / hq;
+        it.h = off - rank * hq;
+        it.b = cb;
+        int s = 0;
+        for (int seen = 0; s < B; ++s)
+            if (blocks_of(len_of(s)) > cb) {
+                if (seen == rank) break;
+                ++seen;
+            }
+        it.start = ld_shared_s32(tab + 8 * s);
+        it.len = len_of(s);
+        it.T = (it.len + kBM - 1) / kBM;
+        return true;
+    }
     __device__ bool resolve(int idx, Item &it, unsigned *err) const {
+        if (kCompact) return resolve_compact(idx, it);
         const int per_block = B * hq;
         it.b = causal ? n_blocks - 1 - idx / per_block : idx / per_block;
         const int rem = idx % per_block;
@@ -215,7 +279,7 @@ __host__ __device__ constexpr uint32_t kmajor_step(int kk) {
 // 64-dim halves are kHalfBytes apart (LBO), 8-key groups 1 KB apart (SBO).
 __host__ __device__ constexpr uint32_t v_step(int kk) { return uint32_t((kk * 2048) >> 4); }
 
-template <bool kVarlen>
+template <bool kVarlen, bool kCompact>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap,
@@ -228,12 +292,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sRing = sQ + kQBytes;
     const uint32_t sStage = sRing + kRingBytes;
-    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + kQBytes + kRingBytes + kStageBytes);
+    int2 *seq_tab = reinterpret_cast<int2 *>(smem + kQBytes + kRingBytes + kStageBytes);
+    uint64_t *bar_mem =
+        reinterpret_cast<uint64_t *>(smem + kQBytes + kRingBytes + kStageBytes + kTabBytes +
+                                     kCursorBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mem + kNumBars);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const Bars bars{smem_u32(bar_mem)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Work<kVarlen> work(cu_seqlens, B, max_len, total, causal, hq, group);
     const int G = gridDim.x, cta = blockIdx.x;
 
     if (threadIdx.x == 0) {
@@ -270,6 +336,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     // (it waits for this grid in the same way).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (kCompact) {  // B <= kCompactBatch (the host's choice)
+        const int max_rows = (((max_len + kBM - 1) / kBM + 1) / 2) * 2 * kBM;
+        for (int s = threadIdx.x; s < B; s += blockDim.x) {
+            const int st = __ldg(cu_seqlens + s), en = __ldg(cu_seqlens + s + 1);
+            int len = en - st;
+            if (st < 0 || len < 0 || en > total || len > max_rows) {
+                atomicOr(err, kErrBadSeqlens);  // malformed: the sequence gets no items
+                len = 0;
+            }
+            seq_tab[s] = make_int2(st, len);
+        }
+        __syncthreads();
+    }
+    const Work<kVarlen, kCompact> work(cu_seqlens, kCompact ? smem_u32(seq_tab) : 0u, B,
+                                       max_len, total, causal, hq,
+                       group);
 
     if (warp >= kSoftmaxWarps) {
         // producer / MMA warpgroup: give registers to the softmax groups
@@ -639,7 +722,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     }
 }
 
-template <bool kVarlen>
+template <bool kVarlen, bool kCompact>
 cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                    void *out, float *lse, const int *cu_seqlens, int B, int max_len, int total,
                    int causal, int hq, int hkv, int num_sms, unsigned *err,
@@ -649,7 +732,7 @@ cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUten
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<kVarlen>,
+        e = cudaFuncSetAttribute(prefill_kernel<kVarlen, kCompact>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -666,7 +749,7 @@ cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUten
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel<kVarlen>, qmap, kmap, vmap,
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kVarlen, kCompact>, qmap, kmap, vmap,
                               static_cast<__nv_bfloat16 *>(out), lse, cu_seqlens, B, max_len,
                               total, causal, hq, hq / hkv, err);
 }
@@ -679,10 +762,17 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            int hq, int hkv, int num_sms, unsigned *err, cudaStream_t stream) {
     // one sequence: the instantiation without per-sequence offsets
     if (cu_seqlens == nullptr)
-        return launch<false>(qmap, kmap, vmap, out, lse, nullptr, 1, total, total, causal, hq,
-                             hkv, num_sms, err, stream);
-    return launch<true>(qmap, kmap, vmap, out, lse, cu_seqlens, B, max_len, total, causal, hq,
-                        hkv, num_sms, err, stream);
+        return launch<false, false>(qmap, kmap, vmap, out, lse, nullptr, 1, total, total,
+                                    causal, hq, hkv, num_sms, err, stream);
+    // A batch whose rows fill batch x max_seqlen has every sequence at the
+    // maximum length, so no empty blocks to skip: the plain order, whose
+    // kernel carries no compact-order code.  Mixed lengths (up to
+    // kCompactBatch sequences) take the compact order.
+    if (B <= kCompactBatch && static_cast<long long>(B) * max_len != total)
+        return launch<true, true>(qmap, kmap, vmap, out, lse, cu_seqlens, B, max_len, total,
+                                  causal, hq, hkv, num_sms, err, stream);
+    return launch<true, false>(qmap, kmap, vmap, out, lse, cu_seqlens, B, max_len, total,
+                               causal, hq, hkv, num_sms, err, stream);
 }
 
 }  // namespace gqa

@@ -62,6 +62,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y,
                  "r"(w)
                  : "memory");
 }
+__device__ __forceinline__ int ld_shared_s32(uint32_t a) {
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"

@@ -86,3 +86,37 @@ def test_varlen_rejects_bad_host_arguments():
         gqa.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda().long(), 20)
     with pytest.raises(gqa.GqaError):
         gqa.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), 0)
+
+
+def _check_sequences(q, k, v, cu, lengths, out, which, n_rows=3):
+    for s in which:
+        n = lengths[s]
+        if n == 0:
+            continue
+        a = int(cu[s])
+        rows = sorted({0, n - 1, n // 2} | set(range(min(n, n_rows))))
+        want = oracle.prefill_rows(q[a:a + n], k[a:a + n], v[a:a + n], rows)
+        assert_close(out[a:a + n][rows].cpu(), want, what=f"seq {s} (len {n})")
+
+
+def test_varlen_uniform_batch_plain_order():
+    """Every sequence at max_seqlen: the plain item order (no empty blocks)."""
+    lengths = [700] * 5
+    q, k, v, cu = packed(lengths, seed=41)
+    out = run(q, k, v, cu, 700)
+    assert gqa.device_error() == 0
+    _check_sequences(q, k, v, cu, lengths, out, range(5))
+
+
+@pytest.mark.parametrize("n_seq", [64, 70])
+def test_varlen_many_mixed_sequences(n_seq):
+    """64 mixed-length sequences use the compact item order (the largest batch
+    it takes), 70 the plain order with empty items."""
+    rng = np.random.default_rng(n_seq)
+    lengths = [int(x) for x in rng.integers(1, 700, n_seq)]
+    lengths[n_seq // 2] = 1500  # one long sequence: many blocks empty for the rest
+    q, k, v, cu = packed(lengths, seed=n_seq)
+    out = run(q, k, v, cu, max(lengths))
+    assert gqa.device_error() == 0
+    assert bool(torch.isfinite(out.float()).all())
+    _check_sequences(q, k, v, cu, lengths, out, [0, 1, n_seq // 2, n_seq - 2, n_seq - 1])
