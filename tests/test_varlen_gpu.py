@@ -120,3 +120,28 @@ def test_varlen_many_mixed_sequences(n_seq):
     assert gqa.device_error() == 0
     assert bool(torch.isfinite(out.float()).all())
     _check_sequences(q, k, v, cu, lengths, out, [0, 1, n_seq // 2, n_seq - 2, n_seq - 1])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_varlen_random_batches(seed):
+    """Random mixed batches (2-64 sequences, lengths 0-1000, causal or not,
+    max_seqlen sometimes above the longest sequence): every sequence's
+    sampled rows against the oracle, and no row left unwritten."""
+    rng = np.random.default_rng(100 + seed)
+    n_seq = int(rng.integers(2, 65))
+    lengths = [int(x) for x in rng.integers(0, 1001, n_seq)]
+    if sum(lengths) == 0:
+        lengths[0] = 5
+    causal = bool(seed % 2 == 0)
+    max_len = max(lengths) + (int(rng.integers(1, 400)) if seed % 3 == 0 else 0)
+    q, k, v, cu = packed(lengths, seed=200 + seed)
+    out = run(q, k, v, cu, max_len, causal=causal)
+    assert gqa.device_error() == 0
+    assert bool(torch.isfinite(out.float()).all())
+    for s, n in enumerate(lengths):
+        if n == 0:
+            continue
+        a = int(cu[s])
+        rows = sorted({0, n - 1, int(rng.integers(0, n))})
+        want = oracle.prefill_rows(q[a:a + n], k[a:a + n], v[a:a + n], rows, causal=causal)
+        assert_close(out[a:a + n][rows].cpu(), want, what=f"seq {s} (len {n})")
