@@ -110,3 +110,30 @@ def test_heads_rejects_unsupported_layouts():
     with pytest.raises(gqa.GqaError) as e:  # 16 query heads per KV head: decode holds 8
         gqa.decode_heads(qd, kd, kd)
     assert e.value.code == 3
+
+
+@pytest.mark.parametrize("hq,hkv,S", [(256, 8, 200), (256, 256, 130)])
+def test_prefill_heads_at_the_head_limit(hq, hkv, S):
+    """256 query heads, the most the entry point takes (groups of 32 and 1)."""
+    q, k, v = qkv(S, hq, hkv, seed=61)
+    out = poisoned((1, S, hq, 128))
+    gqa.prefill_heads(q.cuda(), k.cuda(), v.cuda(), out=out)
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    rows = [0, S // 2, S - 1]
+    assert_close(out[0, rows], oracle.prefill_rows(q, k, v, rows), what=f"prefill {hq}/{hkv}")
+
+
+def test_decode_heads_at_the_head_limit():
+    """256 query heads over 32 KV heads: the largest layout with groups of 8."""
+    hq, hkv, L = 256, 32, 3000
+    q = normal_bf16((2, hq, 128), 71)
+    kc = normal_bf16((2, L, hkv, 128), 72)
+    vc = normal_bf16((2, L, hkv, 128), 73)
+    sl = torch.tensor([L, 1234], dtype=torch.int32, device="cuda")
+    out = poisoned((2, hq, 128))
+    gqa.decode_heads(q.cuda(), kc.cuda(), vc.cuda(), sl, out=out)
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    for b, n in enumerate((L, 1234)):
+        assert_close(out[b].cpu(), oracle.decode(q[b], kc[b, :n], vc[b, :n]), what=f"seq {b}")
