@@ -160,12 +160,11 @@ struct Work {
     __device__ int item(int r, int c, int G) const {
         return r * G + ((r & 1) ? (G - 1 - c) : c);
     }
-    // false: nothing to do for this item (past its sequence, or a malformed
-    // cu array, which also sets kErrBadSeqlens)
-    // Compact order (see above).  The lanes of a warp may interleave their
-    // reads and writes of the cursor slot in any order: all compute the same
-    // state for the same index, and a lane that reads the already advanced
-    // state finds its item in it directly.
+    // Compact order (see above).  The cursor is only a cache: walking from the
+    // initial state is always correct, so the lanes of a warp may interleave
+    // their reads and writes of the slot in any order (all compute the same
+    // state for the same index; a lane that reads an already advanced state
+    // finds its item in it directly).
     __device__ bool resolve_compact(int idx, Item &it) const {
         const uint32_t c = cursor();
         const uint4 cur = ld_shared_v4(c);
@@ -190,6 +189,8 @@ struct Work {
         it.T = (it.len + kBM - 1) / kBM;
         return true;
     }
+    // false: nothing to do for this item (past its sequence, or a malformed
+    // cu array, which also sets kErrBadSeqlens)
     __device__ bool resolve(int idx, Item &it, unsigned *err) const {
         if (kCompact) return resolve_compact(idx, it);
         const int per_block = B * hq;
