@@ -704,7 +704,8 @@ def run_sweep(args):
     cases += [("batched", (8, 8192), False), ("batched", (32, 4096), False),
               ("batched", (128, 2048), False)]
     cases += [("heads", ("prefill", 64, 8, 8192), False), ("heads", ("prefill", 32, 32, 8192), False),
-              ("heads", ("decode", 64, 8, 32768), False), ("heads", ("decode", 32, 32, 16384), False)]
+              ("heads", ("decode", 64, 8, 32768), False), ("heads", ("decode", 32, 32, 16384), False),
+              ("heads", ("decode", 128, 8, 32768), False)]
     for kind, n, stress in cases:
         if kind == "heads":
             print(json.dumps(sweep_heads(*n, dev, peaks, src)), flush=True)

@@ -284,7 +284,7 @@ def prefill_heads(q, k, v, cu_seqlens=None, max_seqlen=None, causal: bool = True
 
 def decode_heads(q, kcache, vcache, seqlens=None, out=None, stream=None,
                  return_lse: bool = False):
-    """Decode for any head layout with at most 8 query heads per KV head:
+    """Decode for any head layout with at most 16 query heads per KV head:
     q [B,Hq,128] against caches [B,Lmax,Hkv,128] bf16; sequence b attends to
     its first seqlens[b] rows (int32 CUDA tensor [B]; None = all Lmax).
     Returns out [B,Hq,128] (and lse [B,Hq] fp32)."""

@@ -34,21 +34,29 @@ constexpr int kTileBytes = 2 * kHalfBytes;       // K (or V) tile, 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;      // K + V, 32 KB
 constexpr int kThreads = (kWarps + 1) * 32;      // + one TMA producer warp
 constexpr int kCtasPerSm = 1;
-// query heads per KV head the kernel handles: the warp MMA's 8 N columns
-constexpr int kMaxGroup = 8;
-constexpr int kCmbFloats = kWarps * kMaxGroup * kD; // cross-warp merge buffer
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + size_t(kStages) * kStageBytes +
-                              size_t(kCmbFloats) * 4 + 2 * kWarps * kMaxGroup * 4 +
-                              2 * kStages * 8;
+// query heads per KV head the kernel handles: up to two N tiles of the warp
+// MMA's 8 columns
+constexpr int kMaxGroup = 16;
+// Shared memory of the instantiation with kNT tiles: the ring, the
+// cross-warp merge buffers for 8 * kNT heads, the barriers.
+constexpr size_t smem_bytes(int nt) {
+    return 1024 /*align slack*/ + size_t(kStages) * kStageBytes +
+           size_t(kWarps) * 8 * nt * kD * 4 + 2 * kWarps * 8 * nt * 4 + 2 * kStages * 8;
+}
+constexpr size_t kSmemBytes = smem_bytes(2);  // the largest
+static_assert(smem_bytes(1) < kSmemBytes, "one-tile instantiations stay smaller");
 
 static_assert(kStageKeys == kDecodeBoxRows, "tensor-map box must match a stage");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kMaxGroup == kDecodeMaxGroup, "host limit and kernel buffers agree");
 
 // log2(e) / sqrt(128): scores are kept in the base-2 domain.
 constexpr float kScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
 
 // kFixedGroup > 0: the query heads per KV head are a compile-time constant
-// (the 32/8 layout); 0: they come from `group_arg` (1..kMaxGroup).
-template <int kFixedGroup>
+// (the 32/8 layout); 0: they come from `group_arg` (1..8 * kNT).  kNT: N
+// tiles of 8 query heads per MMA step (1, or 2 for groups of 9..16).
+template <int kFixedGroup, int kNT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
@@ -56,13 +64,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     int Lmax, int chunk, int hq, int group_arg, float *__restrict__ part_o,
                     float *__restrict__ part_lse, unsigned *err) {
     const int group = kFixedGroup > 0 ? kFixedGroup : group_arg;
+    constexpr int kMG = 8 * kNT;  // heads the merge buffers hold
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *cmb_o = reinterpret_cast<float *>(smem + kStages * kStageBytes);
-    float *cmb_m = cmb_o + kCmbFloats;
-    float *cmb_l = cmb_m + kWarps * kMaxGroup;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(cmb_l + kWarps * kMaxGroup);
+    float *cmb_m = cmb_o + kWarps * kMG * kD;
+    float *cmb_l = cmb_m + kWarps * kMG;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cmb_l + kWarps * kMG);
     const uint32_t tiles = smem_u32(smem);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
 
@@ -130,30 +139,43 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 
     // -------------------------------------------------------- compute warps
-    // Mapping (m16n8k16 fragments, gi = lane/4, ti = lane%4):
-    //   S^T[key][head] = K[key][d] . Q^T[d][head]   (A = K via ldmatrix,
-    //   B = the 4 query heads of this group in columns 0..3, 4..7 zero)
+    // Mapping (m16n8k16 fragments, gi = lane/4, ti = lane%4), per N tile nt
+    // of 8 query heads (group heads nt*8 .. nt*8+7; kNT tiles hold groups of
+    // up to 8 * kNT, missing heads are zero columns):
+    //   S^T[key][head] = K[key][d] . Q^T[d][head]   (A = K via ldmatrix, B = Q^T)
     //   O^T[d][head]  += V^T[d][key] . P^T[key][head]  (A = V^T via
     //   ldmatrix.trans, B = P^T from the S^T fragment by movmatrix.trans)
-    // A lane owns heads 2ti and 2ti+1 in both products, so the running max,
-    // sum and O rescale stay in registers.
+    // Every K and V fragment loaded from shared memory serves all N tiles.
+    // A lane owns heads nt*8 + 2ti and nt*8 + 2ti + 1 in both products, so the
+    // running max, sum and O rescale stay in registers.
     const int gi = lane >> 2, ti = lane & 3;
-    uint32_t qf[8][2];
+    uint32_t qf[kNT][8][2];
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        if (gi < group) {
-            const uint32_t *qh = reinterpret_cast<const uint32_t *>(
-                q + (g * group + gi) * kD + 16 * kk + 2 * ti);
-            qf[kk][0] = __ldg(qh);
-            qf[kk][1] = __ldg(qh + 4);
-        } else {
-            qf[kk][0] = qf[kk][1] = 0u;
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int hg = nt * 8 + gi;  // head of this B column inside the group
+            if (hg < group) {
+                const uint32_t *qh = reinterpret_cast<const uint32_t *>(
+                    q + (g * group + hg) * kD + 16 * kk + 2 * ti);
+                qf[nt][kk][0] = __ldg(qh);
+                qf[nt][kk][1] = __ldg(qh + 4);
+            } else {
+                qf[nt][kk][0] = qf[nt][kk][1] = 0u;
+            }
         }
-    }
-    float o[8][4];
+    float o[kNT][8][4];
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    float m[kNT][2], l[kNT][2];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+    }
     const int kb = warp * 16;  // this warp's 16 keys inside a stage
 
     for (int it = 0; it < n_iter; ++it) {
@@ -161,7 +183,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         if (!mbar_wait(full0 + 8 * s, (it / kStages) & 1, err, kErrWaitFull)) break;
         const uint32_t kt = tiles + s * kStageBytes, vt = kt + kTileBytes;
 
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+        float c[kNT][4];
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
         {
             const uint32_t row = kb + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
@@ -169,39 +193,46 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(sw128(kt + (kk >> 2) * kHalfBytes, row, 2 * (kk & 3) + (lane >> 4)),
                         a0, a1, a2, a3);
-                mma_bf16_16816(c0, c1, c2, c3, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt)
+                    mma_bf16_16816(c[nt][0], c[nt][1], c[nt][2], c[nt][3], a0, a1, a2, a3,
+                                   qf[nt][kk][0], qf[nt][kk][1]);
             }
         }
         const int key_a = key0 + it * kStageKeys + kb + gi, key_b = key_a + 8;
-        float x0 = c0 * kScaleLog2, x1 = c1 * kScaleLog2;
-        float x2 = c2 * kScaleLog2, x3 = c3 * kScaleLog2;
-        if (key_a >= L) x0 = x1 = -INFINITY;
-        if (key_b >= L) x2 = x3 = -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        uint32_t b[kNT][2];
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float r0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked
-        const float r1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
-        const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1);
-        const float p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
+        for (int nt = 0; nt < kNT; ++nt) {
+            float x0 = c[nt][0] * kScaleLog2, x1 = c[nt][1] * kScaleLog2;
+            float x2 = c[nt][2] * kScaleLog2, x3 = c[nt][3] * kScaleLog2;
+            if (key_a >= L) x0 = x1 = -INFINITY;
+            if (key_b >= L) x2 = x3 = -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+            const float r0 = mn0 == -INFINITY ? 0.f : mn0;  // all keys so far masked
+            const float r1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = ex2(m[nt][0] - r0), al1 = ex2(m[nt][1] - r1);
+            const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1);
+            const float p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
+            l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+            l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[nt][mt][0] *= al0;
+                o[nt][mt][1] *= al1;
+                o[nt][mt][2] *= al0;
+                o[nt][mt][3] *= al1;
+            }
+            b[nt][0] = movmatrix_t(pack_bf16(p0, p1));  // keys 0..7
+            b[nt][1] = movmatrix_t(pack_bf16(p2, p3));  // keys 8..15
         }
-        const uint32_t b0 = movmatrix_t(pack_bf16(p0, p1));  // keys 0..7
-        const uint32_t b1 = movmatrix_t(pack_bf16(p2, p3));  // keys 8..15
         {
             const int mi = lane >> 3;
             const uint32_t row = kb + (lane & 7) + (mi >> 1) * 8;
@@ -210,7 +241,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int dc = 2 * mt + (mi & 1);  // 16-byte chunk along d
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(sw128(vt + (dc >> 3) * kHalfBytes, row, dc & 7), a0, a1, a2, a3);
-                mma_bf16_16816(o[mt][0], o[mt][1], o[mt][2], o[mt][3], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt)
+                    mma_bf16_16816(o[nt][mt][0], o[nt][mt][1], o[nt][mt][2], o[nt][mt][3], a0,
+                                   a1, a2, a3, b[nt][0], b[nt][1]);
             }
         }
         __syncwarp();
@@ -231,27 +265,30 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 
     // ------------------------------------------- merge the 4 warps' states
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    if (2 * ti < group) {  // lane owns query heads 2ti and 2ti+1 of the group
-        const int h0 = 2 * ti, h1 = 2 * ti + 1;
-        float *w0 = cmb_o + (warp * kMaxGroup + h0) * kD;
-        float *w1 = cmb_o + (warp * kMaxGroup + h1) * kD;
+    for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int d = 16 * mt + gi;
-            w0[d] = o[mt][0];
-            w1[d] = o[mt][1];
-            w0[d + 8] = o[mt][2];
-            w1[d + 8] = o[mt][3];
+        for (int off = 4; off < 32; off <<= 1) {
+            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
         }
-        if (gi == 0) {
-            cmb_m[warp * kMaxGroup + h0] = m0;
-            cmb_m[warp * kMaxGroup + h1] = m1;
-            cmb_l[warp * kMaxGroup + h0] = l0;
-            cmb_l[warp * kMaxGroup + h1] = l1;
+        const int h0 = nt * 8 + 2 * ti, h1 = h0 + 1;  // this lane's heads in the group
+        if (h0 < group) {
+            float *w0 = cmb_o + (warp * kMG + h0) * kD;
+            float *w1 = cmb_o + (warp * kMG + h1) * kD;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int d = 16 * mt + gi;
+                w0[d] = o[nt][mt][0];
+                w1[d] = o[nt][mt][1];
+                w0[d + 8] = o[nt][mt][2];
+                w1[d + 8] = o[nt][mt][3];
+            }
+            if (gi == 0) {
+                cmb_m[warp * kMG + h0] = m[nt][0];
+                cmb_m[warp * kMG + h1] = m[nt][1];
+                cmb_l[warp * kMG + h0] = l[nt][0];
+                cmb_l[warp * kMG + h1] = l[nt][1];
+            }
         }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");
@@ -261,15 +298,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int n = t >> 5; n < group; n += kWarps) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmb_m[w * kMaxGroup + n]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cmb_m[w * kMG + n]);
         float den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float mw = cmb_m[w * kMaxGroup + n];
+            const float mw = cmb_m[w * kMG + n];
             const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-            den += f * cmb_l[w * kMaxGroup + n];
+            den += f * cmb_l[w * kMG + n];
             const float4 v =
-                *reinterpret_cast<const float4 *>(cmb_o + (w * kMaxGroup + n) * kD + d0);
+                *reinterpret_cast<const float4 *>(cmb_o + (w * kMG + n) * kD + d0);
             acc[0] += f * v.x;
             acc[1] += f * v.y;
             acc[2] += f * v.z;
@@ -406,12 +443,17 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<kGroup>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        e = cudaFuncSetAttribute(decode_split_kernel<kGroup, 1>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_bytes(1)));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_split_kernel<0>,
+            e = cudaFuncSetAttribute(decode_split_kernel<0, 1>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     int(kSmemBytes));
+                                     int(smem_bytes(1)));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_split_kernel<0, 2>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(smem_bytes(2)));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -428,12 +470,14 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.n_split, plan.hkv, plan.batch);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes(group <= 8 ? 1 : 2);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, group == kGroup ? decode_split_kernel<kGroup>
-                                                 : decode_split_kernel<0>,
+    e = cudaLaunchKernelEx(&cfg,
+                           group == kGroup ? decode_split_kernel<kGroup, 1>
+                           : group <= 8    ? decode_split_kernel<0, 1>
+                                           : decode_split_kernel<0, 2>,
                            kmap, vmap, static_cast<const __nv_bfloat16 *>(q), seqlens, Lmax,
                            plan.chunk, plan.hq, group, part_o, part_lse, err);
     if (e != cudaSuccess) return e;

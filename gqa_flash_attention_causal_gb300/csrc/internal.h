@@ -25,7 +25,7 @@ struct DecodePlan {
     int hq = kHq;
     int hkv = kHkv;
 };
-constexpr int kDecodeMaxGroup = 8;  // query heads per KV head the decode supports
+constexpr int kDecodeMaxGroup = 16;  // query heads per KV head the decode supports
 DecodePlan decode_plan(int Lmax, int batch, int num_sms, int hq = kHq, int hkv = kHkv);
 size_t decode_workspace_bytes(const DecodePlan &p);
 

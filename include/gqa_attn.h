@@ -160,9 +160,9 @@ gqa_status gqa_attn_decode_batched(const void *q, const void *kcache,
  *     q, out [batch][num_q_heads][128],  caches [batch][max_len][num_kv_heads][128]
  * bf16, lse (may be NULL) [batch][num_q_heads] fp32.  The query heads of a
  * KV head are computed together from one pass over its cache, which holds
- * at most 8 of them: 1 <= num_kv_heads <= num_q_heads <= 256,
+ * at most 16 of them: 1 <= num_kv_heads <= num_q_heads <= 256,
  * num_q_heads a multiple of num_kv_heads and num_q_heads / num_kv_heads
- * <= 8; otherwise GQA_ERR_SHAPE.
+ * <= 16; otherwise GQA_ERR_SHAPE.
  */
 gqa_status gqa_attn_decode_heads(const void *q, const void *kcache,
                                  const void *vcache, void *out, float *lse,

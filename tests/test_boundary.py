@@ -70,8 +70,8 @@ def test_bad_head_counts_rejected_without_device(lib):
                                           None) == 3, (hq, hkv)
         assert lib.gqa_attn_decode_heads(p, p, p, p, None, None, 1, 64, hq, hkv,
                                          None) == 3, (hq, hkv)
-    # decode holds at most 8 query heads per KV head
-    for hq, hkv in ((32, 2), (16, 1), (72, 8)):
+    # decode holds at most 16 query heads per KV head
+    for hq, hkv in ((64, 2), (32, 1), (136, 8)):
         assert lib.gqa_attn_decode_heads(p, p, p, p, None, None, 1, 64, hq, hkv, None) == 3
     # a single sequence (no cu_seqlens) must have batch 1 and max_seqlen == total
     assert lib.gqa_attn_prefill_heads(p, p, p, p, None, None, 2, 64, 128, 32, 8, 1, None) == 3

@@ -1,6 +1,6 @@
 """Other head layouts (query heads a multiple of KV heads) against the fp64
-oracle: multi-head (Hkv = Hq), multi-query (Hkv = 1, prefill), every decode
-group from 1 to 8, single sequences and packed batches."""
+oracle: multi-head (Hkv = Hq), multi-query (Hkv = 1), every decode
+group from 1 to 8 plus 9, 12 and 16, single sequences and packed batches."""
 import numpy as np
 import pytest
 import torch
@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 # (query heads, KV heads)
 PREFILL_LAYOUTS = [(32, 8), (64, 8), (32, 32), (16, 1), (28, 4), (14, 2), (7, 7), (40, 5)]
 DECODE_LAYOUTS = [(32, 8), (64, 8), (32, 32), (8, 1), (28, 4), (16, 8), (12, 4), (48, 8),
-                  (10, 2), (16, 4), (64, 16)]
+                  (10, 2), (16, 4), (64, 16), (128, 8), (16, 1), (36, 3), (9, 1)]
 
 
 def qkv(S, hq, hkv, seed=21):
@@ -106,8 +106,8 @@ def test_heads_rejects_unsupported_layouts():
         gqa.prefill_heads(q, k, k)
     assert e.value.code == 3
     qd = torch.zeros((1, 32, 128), dtype=torch.bfloat16, device="cuda")
-    kd = torch.zeros((1, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(gqa.GqaError) as e:  # 16 query heads per KV head: decode holds 8
+    kd = torch.zeros((1, 64, 1, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(gqa.GqaError) as e:  # 32 query heads per KV head: decode holds 16
         gqa.decode_heads(qd, kd, kd)
     assert e.value.code == 3
 
