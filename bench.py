@@ -706,6 +706,8 @@ def run_sweep(args):
     cases += [("heads", ("prefill", 64, 8, 8192), False), ("heads", ("prefill", 32, 32, 8192), False),
               ("heads", ("decode", 64, 8, 32768), False), ("heads", ("decode", 32, 32, 16384), False),
               ("heads", ("decode", 128, 8, 32768), False)]
+    # ragged sizes (a partial last 128-row tile / 64-key stage): tails at full speed?
+    cases += [("prefill", 12345, False), ("decode", 50001, False)]
     for kind, n, stress in cases:
         if kind == "heads":
             print(json.dumps(sweep_heads(*n, dev, peaks, src)), flush=True)
@@ -783,6 +785,8 @@ def run_sweep(args):
         err = np.abs(got - want)
         scale = float(v.float().abs().max()) if kind.startswith("prefill") and stress else (
             float(vc.float().abs().max()) if stress else 1.0)
+        if (kind == "prefill" and n % 128) or (kind == "decode" and n % 64):
+            line["workload"] += "_tail"
         line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
                      "tolerance_scale": scale,
                      "parity_ok": bool(err.max() <= 2e-2 * scale and err.mean() <= 2e-3 * scale),
