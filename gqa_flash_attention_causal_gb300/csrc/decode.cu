@@ -22,6 +22,8 @@
 // FMAs, which keeps instruction issue far below the memory time.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -101,6 +103,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == kWarps * 32) {
         prefetch_tmap(&kmap);
         prefetch_tmap(&vmap);
+        // Start this CTA's first stages on their way into L2 while the
+        // preceding kernel finishes.  A prefetch only fills L2, the point of
+        // coherence every SM reads through, so it cannot hand out data older
+        // than what that kernel writes; the loads into shared memory still
+        // wait for it below.  With per-sequence lengths (known only after
+        // the wait) nothing is prefetched.
+        if (seqlens == nullptr) {
+            const int k0 = split * chunk;
+            const int n_pre =
+                min(kStages, (min(Lmax, k0 + chunk) - k0 + kStageKeys - 1) / kStageKeys);
+            for (int it = 0; it < n_pre; ++it) {
+                const int row = row0 + k0 + it * kStageKeys;
+                tma_prefetch_3d(&kmap, 0, g, row);
+                tma_prefetch_3d(&kmap, 64, g, row);
+                tma_prefetch_3d(&vmap, 0, g, row);
+                tma_prefetch_3d(&vmap, 64, g, row);
+            }
+        }
     }
     __syncthreads();
     // Launched as a programmatic dependent of whatever kernel precedes it on
@@ -335,8 +355,11 @@ decode_combine_kernel(const float *__restrict__ part_o,
                       const float *__restrict__ part_lse, int n_split, int hq,
                       __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
                       const int *__restrict__ seqlens, int Lmax) {
-    // Launched as a programmatic dependent of the split kernel: wait until
-    // its results are visible.
+    // The next kernel on the stream may be scheduled now (it waits for this
+    // grid's completion before touching its results).  This kernel is a
+    // programmatic dependent of the split kernel: wait until its results are
+    // visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float s_m[kCmbWarps], s_den[kCmbWarps];
     __shared__ float4 s_acc[kCmbWarps][32];
@@ -440,25 +463,29 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap,
                           const void *q, void *out, float *lse, const int *seqlens, int Lmax,
                           const DecodePlan &plan, void *workspace, unsigned *err,
                           cudaStream_t stream) {
-    static bool configured[kMaxDevices] = {};  // the attribute is per device
+    // The shared-memory attribute is per device: set once per device, by
+    // whichever host thread gets there first (the others wait for it).
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<kGroup, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem_bytes(1)));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_split_kernel<0, 1>,
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        cudaError_t r = cudaFuncSetAttribute(decode_split_kernel<kGroup, 1>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem_bytes(1)));
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(decode_split_kernel<0, 1>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      int(smem_bytes(1)));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_split_kernel<0, 2>,
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(decode_split_kernel<0, 2>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      int(smem_bytes(2)));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+        configured[dev] = r;
+    });
+    if ((e = configured[dev]) != cudaSuccess) return e;
     const int group = plan.hq / plan.hkv;
     float *part_o = static_cast<float *>(workspace);
     float *part_lse = part_o + size_t(plan.n_split) * plan.batch * plan.hq * kD;

@@ -45,6 +45,8 @@
 // memory and writes them as 128-byte row segments.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -728,16 +730,20 @@ cudaError_t launch(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUten
                    void *out, float *lse, const int *cu_seqlens, int B, int max_len, int total,
                    int causal, int hq, int hkv, int num_sms, unsigned *err,
                    cudaStream_t stream) {
-    static bool configured[kMaxDevices] = {};
+    // The shared-memory attribute is per device: set once per device, by
+    // whichever host thread gets there first (the others wait for it).
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices && !configured[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<kVarlen, kCompact>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev] {
+        configured[dev] = cudaFuncSetAttribute(prefill_kernel<kVarlen, kCompact>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               int(kSmemBytes));
+    });
+    if ((e = configured[dev]) != cudaSuccess) return e;
     const long long n_items = ((max_len + kBM - 1) / kBM + 1) / 2 * (long long)B * hq;
     const int grid = n_items < num_sms ? int(n_items) : num_sms;
     cudaLaunchAttribute attr[1];

@@ -129,6 +129,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m,
         "l"(policy)
         : "memory");
 }
+// Prefetch the same 3-D tile into L2 only: no shared memory is written and no
+// barrier is signalled.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
 
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,

@@ -42,3 +42,24 @@ def sample_rows(S: int, n_random: int = 24, seed: int = 0):
     rng = np.random.default_rng(seed)
     rows.update(int(x) for x in rng.integers(0, S, size=n_random))
     return sorted(r for r in rows if 0 <= r < S)
+
+
+TILE = 128  # query rows per tile of the prefill kernel (two tiles per work item)
+
+
+def tile_rows(S: int, seed: int = 0):
+    """Rows that put every 128-row query tile under comparison: its first
+    row, its last row and one random row inside it.  Every 256-row work item
+    (both of its tiles) and, with all heads compared, every (item, head)
+    pair of a single-sequence prefill is then checked element by element."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for t0 in range(0, S, TILE):
+        t1 = min(S, t0 + TILE) - 1
+        rows.update((t0, t1, int(rng.integers(t0, t1 + 1))))
+    return sorted(rows)
+
+
+def covered_tiles(rows, S: int) -> int:
+    """Number of distinct 128-row query tiles that contain one of `rows`."""
+    return len({r // TILE for r in rows if 0 <= r < S})

@@ -1,7 +1,8 @@
 """Parity at the bench's full sizes, in the launch configuration bench.py
 times: one CUDA graph replaying the causal prefill at S=32768, one replaying
-the decode at L=65536 with a caller workspace; sampled rows against the
-oracle."""
+the decode at L=65536 with a caller workspace.  The prefill is compared with
+the oracle on the first, the last and a random row of every 128-row query
+tile (768 rows, all heads), the decode in full."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,7 @@ import torch
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
 from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
-from tests.parity import assert_close, sample_rows
+from tests.parity import assert_close, covered_tiles, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +42,7 @@ def test_bench_step_graph_replay_matches_oracle():
     torch.cuda.synchronize()
     assert gqa.device_error() == 0
     assert bool(torch.isfinite(out.float()).all())
-    rows = sample_rows(S, n_random=16, seed=3)
+    rows = sorted(set(sample_rows(S, n_random=16, seed=3)) | set(tile_rows(S, seed=3)))
+    assert covered_tiles(rows, S) == S // 128
     assert_close(out[0, rows], oracle.prefill_rows(q, k, v, rows), what="bench prefill")
     assert_close(dout, oracle.decode(dq, kc, vc), what="bench decode")

@@ -6,7 +6,8 @@ import torch
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
 from gqa_flash_attention_causal_gb300.inputs import prefill_inputs
-from tests.parity import assert_close, poisoned, sample_rows, tolerance_scale
+from tests.parity import (assert_close, covered_tiles, poisoned, sample_rows, tile_rows,
+                          tolerance_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,8 +41,12 @@ def test_prefill_noncausal_full(S):
 
 @pytest.mark.parametrize("S", SAMPLED)
 def test_prefill_causal_sampled(S):
+    """The first, the last and a random row of every 128-row query tile, all
+    32 heads, element by element: every (256-row item, head) pair the kernel
+    schedules is compared, not only a few rows of the sequence."""
     (q, k, v), out = run(S)
-    rows = sample_rows(S)
+    rows = sorted(set(sample_rows(S)) | set(tile_rows(S, seed=S)))
+    assert covered_tiles(rows, S) == S // 128
     want = oracle.prefill_rows(q, k, v, rows, causal=True)
     assert_close(out[0, rows], want, what=f"causal S={S} sampled")
     assert bool(torch.isfinite(out.float()).all()), "unwritten output rows"
@@ -49,7 +54,7 @@ def test_prefill_causal_sampled(S):
 
 def test_prefill_stress_s4096():
     (q, k, v), out = run(4096, stress=True)
-    rows = sample_rows(4096, n_random=64)
+    rows = sorted(set(sample_rows(4096, n_random=64)) | set(tile_rows(4096, seed=7)))
     want = oracle.prefill_rows(q, k, v, rows, causal=True)
     assert_close(out[0, rows], want, scale=tolerance_scale(v, True), what="stress")
 
@@ -87,9 +92,14 @@ def test_prefill_running_max_paths(causal, ramp):
     up by far more than the lazy-rescale threshold (2^8) at every KV tile, so
     O and l are rescaled tile after tile; shrinking keys keep the maximum in
     the first tile, so later tiles contribute weights near 2^-large.  Both
-    must match the oracle over full rows.  The scores are large (q x4, keys
-    up to x11), so attention is peaked and |out| approaches max|v|: the
-    large-magnitude rule applies (both bounds times max|v|)."""
+    must match the oracle over full rows.
+
+    Tolerance: q x4 and keys x1..x11 make scores of up to about +-100, so
+    these are large-magnitude inputs and the max-abs bound takes the stress
+    rule (times max|v|): attention this peaked returns single v rows, whose
+    bf16 rounding alone reaches half an ulp of |v| ~ 5 (0.0156), and the
+    measured maximum is 2.15e-2 (non-causal, growing keys).  The mean-abs
+    bound stays the plain 2e-3 (measured at most 7.4e-4)."""
     from gqa_flash_attention_causal_gb300.inputs import normal_bf16
     S = 1024
     q = normal_bf16((1, S, 32, 128), 11, 4.0)
@@ -104,6 +114,7 @@ def test_prefill_running_max_paths(causal, ramp):
     assert gqa.device_error() == 0
     mx, mean = assert_close(out, oracle.prefill(q, k, v, causal=causal)[None],
                             scale=tolerance_scale(v, True), what=f"{ramp} keys, causal={causal}")
+    assert mean <= 2e-3, f"mean abs err {mean:.3e} > 2e-3"
     # the bf16 rounding of a peaked output dominates: still well inside 1 % of max|v|
     assert mx <= 0.01 * tolerance_scale(v, True)
 

@@ -7,7 +7,7 @@ import torch
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
 from gqa_flash_attention_causal_gb300.inputs import normal_bf16, prefill_inputs
-from tests.parity import assert_close, sample_rows
+from tests.parity import assert_close, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,8 @@ def test_varlen_long_mixed_batch_sampled():
     assert gqa.device_error() == 0
     for s, n in enumerate(lengths):
         a = int(cu[s])
-        rows = sample_rows(n, n_random=8, seed=s)
+        # every 128-row tile of every sequence (compact item order)
+        rows = sorted(set(sample_rows(n, n_random=8, seed=s)) | set(tile_rows(n, seed=s)))
         want = oracle.prefill_rows(q[a:a + n], k[a:a + n], v[a:a + n], rows)
         scale = float(v[a:a + n].float().abs().max())
         assert_close(out[a:a + n][rows].cpu(), want, scale=scale, what=f"seq {s}")
