@@ -32,6 +32,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# CUDA feeds each stream to the GPU through one of a few hardware work queues
+# (8 by default), assigned round-robin as streams are created; two streams
+# that share a queue run strictly in submission order.  The end-to-end leg
+# overlaps copies on two streams with kernels on a third, so it asks for the
+# maximum number of queues (read when the CUDA context is created).
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 S_PREFILL = 32768
 L_DECODE = 65536
 HQ, HKV, D = 32, 8, 128
@@ -410,7 +417,10 @@ def run_ours(args, world, rank, local):
     d_out = [(out, dout), (torch.empty_like(out), torch.empty_like(dout))]
     h2d = sum(t.numel() * t.element_size() for t in h_in[0])
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    # kernels and both copy directions on three streams created back to back,
+    # so that round-robin queue assignment gives each its own hardware queue
+    s_cmp, s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    s_cmp.wait_stream(stream)
 
     def e2e_run(steps, pipelined, timeline=None):
         """ms per step; with `timeline` (a list), also the start and end of
@@ -429,9 +439,9 @@ def run_ours(args, world, rank, local):
             e.record(strm)
             return e
 
-        e0.record(stream)
-        s_h2d.wait_stream(stream)
-        s_d2h.wait_stream(stream)
+        e0.record(s_cmp)
+        s_h2d.wait_stream(s_cmp)
+        s_d2h.wait_stream(s_cmp)
         for i in range(steps):
             b = i % 2 if pipelined else 0
             with torch.cuda.stream(s_h2d):
@@ -443,15 +453,16 @@ def run_ours(args, world, rank, local):
                 m.append(mark(s_h2d, i))
                 ready = torch.cuda.Event()
                 ready.record(s_h2d)
-            stream.wait_event(ready)
+            s_cmp.wait_event(ready)
             if done_d2h[b] is not None:
-                stream.wait_event(done_d2h[b])  # outputs of step i-2 are copied out
-            m.append(mark(stream, i))
-            gqa.prefill(d_in[b][0], d_in[b][1], d_in[b][2], causal=True, out=d_out[b][0])
-            gqa.decode(d_in[b][3], d_in[b][4], d_in[b][5], out=d_out[b][1])
-            m.append(mark(stream, i))
+                s_cmp.wait_event(done_d2h[b])  # outputs of step i-2 are copied out
+            m.append(mark(s_cmp, i))
+            with torch.cuda.stream(s_cmp):
+                gqa.prefill(d_in[b][0], d_in[b][1], d_in[b][2], causal=True, out=d_out[b][0])
+                gqa.decode(d_in[b][3], d_in[b][4], d_in[b][5], out=d_out[b][1])
+            m.append(mark(s_cmp, i))
             done_compute[b] = torch.cuda.Event()
-            done_compute[b].record(stream)
+            done_compute[b].record(s_cmp)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(done_compute[b])
                 m.append(mark(s_d2h, i))
@@ -463,9 +474,9 @@ def run_ours(args, world, rank, local):
             if m[0] is not None:
                 marks.append(m)
             if not pipelined:
-                stream.wait_event(done_d2h[b])
-        stream.wait_stream(s_d2h)
-        e1.record(stream)
+                s_cmp.wait_event(done_d2h[b])
+        s_cmp.wait_stream(s_d2h)
+        e1.record(s_cmp)
         torch.cuda.synchronize()
         if timeline is not None:
             for m in marks:
