@@ -35,6 +35,7 @@ SIGNATURES = {
     "gqa_attn_decode_batched": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gqa_attn_prefill_heads": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gqa_attn_decode_heads": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "gqa_attn_prefill_pair": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "gqa_attn_decode": (_I, [_P, _P, _P, _P, _I, _P]),
     "gqa_attn_decode_workspace_bytes": (_S, [_I]),
     "gqa_attn_decode_ws": (_I, [_P, _P, _P, _P, _I, _P, _S, _P]),
@@ -155,6 +156,25 @@ def prefill(q, k, v, causal: bool = True, out=None, stream=None, return_lse: boo
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), S,
         1 if causal else 0, _stream(stream)))
     return out
+
+
+def prefill_pair(q, k, v, causal: bool = True, out=None, stream=None,
+                 return_lse: bool = False):
+    """``prefill`` computed by the paired-CTA kernel (two CTAs per TPC share
+    every K/V tile through cta_group::2 MMAs).  Same arguments and result."""
+    import torch
+    S = q.shape[1]
+    _expect(q, (1, S, HQ, HEAD_DIM), "q")
+    _expect(k, (1, S, HKV, HEAD_DIM), "k")
+    _expect(v, (1, S, HKV, HEAD_DIM), "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _expect(out, (1, S, HQ, HEAD_DIM), "out")
+    lse = torch.empty((1, HQ, S), dtype=torch.float32, device=q.device) if return_lse else None
+    _check("gqa_attn_prefill_pair", lib().gqa_attn_prefill_pair(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, S, 1 if causal else 0, _stream(stream)))
+    return (out, lse) if return_lse else out
 
 
 def prefill_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True, out=None,

@@ -294,6 +294,30 @@ gqa_status gqa_attn_prefill_heads(const void *q, const void *k, const void *v, v
                         num_q_heads, num_kv_heads, stream);
 }
 
+gqa_status gqa_attn_prefill_pair(const void *q, const void *k, const void *v, void *out,
+                                 float *lse, int S, int causal, cudaStream_t stream) {
+    if (!q || !k || !v || !out) return GQA_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
+        return GQA_ERR_ALIGN;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return GQA_ERR_ALIGN;
+    if (S < 1 || S > kMaxPrefillLen) return GQA_ERR_SHAPE;
+    DeviceState *dev = nullptr;
+    gqa_status st = current_device(&dev);
+    if (st != GQA_OK) return st;
+    for (const void *p : {q, k, v, static_cast<const void *>(out)}) {
+        st = check_device_ptr(p);
+        if (st != GQA_OK) return st;
+    }
+    if (lse && (st = check_device_ptr(lse)) != GQA_OK) return st;
+    CUtensorMap qmap, kmap, vmap;
+    st = encode_bshd(&qmap, q, S, kHq, gqa::kPrefillBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&kmap, k, S, kHkv, gqa::kPairKBoxRows);
+    if (st == GQA_OK) st = encode_bshd(&vmap, v, S, kHkv, gqa::kPrefillBoxRows);
+    if (st != GQA_OK) return st;
+    return from_cuda(gqa::launch_prefill_pair(qmap, kmap, vmap, out, lse, S, causal ? 1 : 0,
+                                              kHq, kHkv, dev->err, stream));
+}
+
 size_t gqa_attn_decode_workspace_bytes(int L) {
     if (L < 1 || L > kMaxDecodeLen) return 0;
     DeviceState *dev = nullptr;

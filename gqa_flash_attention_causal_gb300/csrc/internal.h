@@ -54,6 +54,15 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap,
                            const int *cu_seqlens, int B, int max_len, int total, int causal,
                            int hq, int hkv, int num_sms, unsigned *err, cudaStream_t stream);
 
+// Paired-CTA prefill of one sequence (prefill_pair.cu): q, out [S][hq][128],
+// k, v [S][hkv][128]; the tensor maps' boxes are kPrefillBoxRows rows for q
+// and v and kPairKBoxRows rows for k.  lse as for launch_prefill.
+constexpr int kPairKBoxRows = 64;
+cudaError_t launch_prefill_pair(const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                const CUtensorMap &vmap, void *out, float *lse, int S,
+                                int causal, int hq, int hkv, unsigned *err,
+                                cudaStream_t stream);
+
 // ------------------------------------------------------------------ self-test
 // Error bit the self-test kernel's deliberately expiring wait sets.
 constexpr unsigned kErrSelfTestBit = 1u << 31;

@@ -116,6 +116,21 @@ gqa_status gqa_attn_prefill_heads(const void *q, const void *k, const void *v,
                                   cudaStream_t stream);
 
 /*
+ * gqa_attn_prefill (and, with lse non-NULL, gqa_attn_prefill_lse) computed by
+ * the paired-CTA kernel: the CTAs run as clusters of two on the two SMs of a
+ * TPC, and every tcgen05 MMA spans both SMs' tensor memory (M = 256 rows,
+ * 128 per CTA), each CTA staging half of every K and V tile, so that the
+ * pair reads each K/V tile into shared memory once (chowfi/kernels README,
+ * "What helped most", item 2: read K and V once for every group of rows that
+ * needs them).  Same arguments, layouts, result and limits as
+ * gqa_attn_prefill_lse with lse optional; the result agrees with
+ * gqa_attn_prefill's up to the order of fp32 accumulation.
+ */
+gqa_status gqa_attn_prefill_pair(const void *q, const void *k, const void *v,
+                                 void *out, float *lse, int S, int causal,
+                                 cudaStream_t stream);
+
+/*
  * Decode: one query token against a KV cache of length L (every cached
  * position is attended).  q, out: [1][1][32][128] bf16; kcache, vcache:
  * [1][L][8][128] bf16; 1 <= L <= 2^26.
