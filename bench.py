@@ -785,6 +785,7 @@ def run_sweep(args):
     cases = [("prefill", S, False) for S in (512, 2048, 4096, 8192, 16384, 32768)]
     cases += [("prefill", 4096, True)]
     cases += [("prefill_full", S, False) for S in (4096, 16384)]
+    cases += [("prefill_pair", S, False) for S in (4096, 16384, 32768)]
     cases += [("decode", L, False) for L in (2048, 4096, 8192, 16384, 32768, 65536)]
     cases += [("decode", 32768, True)]
     cases += [("varlen", (4096,) * 8, False), ("varlen", (8192, 4096, 2048, 1024, 512, 256), False)]
@@ -803,11 +804,12 @@ def run_sweep(args):
             print(json.dumps(sweep_batch(kind, n, dev, peaks, src)), flush=True)
             continue
         if kind.startswith("prefill"):
-            causal = kind == "prefill"
+            causal = kind != "prefill_full"
+            fn = gqa.prefill_pair if kind == "prefill_pair" else gqa.prefill
             q, k, v = prefill_inputs(n, stress=stress)
             dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
             out = torch.empty_like(dq)
-            call = lambda: gqa.prefill(dq, dk, dv, causal=causal, out=out)  # noqa: E731
+            call = lambda: fn(dq, dk, dv, causal=causal, out=out)  # noqa: E731
             ms_eager = sweep_time(call)[0]
             # GPU time per call: a CUDA graph of back-to-back calls (at small
             # S a single eager call is dominated by the host-side launch path)
