@@ -614,6 +614,17 @@ def timed_parity(oracle_last, out, dout):
                     "CPU baseline"}
 
 
+def rotation_copies(l2_bytes: int, cache_bytes: int) -> int:
+    """KV-cache copies a decode timing loop rotates through so that every
+    call reads its cache from DRAM.  Between two reads of one copy the other
+    copies stream at least 6x the L2 size: with only 2x (as first used), an
+    ncu capture of the rotation found launches at L=32768 and 65536 that
+    read 23 % and 10 % of their cache from L2, whose replacement is not
+    strict LRU; from 5 copies at L=65536 every launch read the full
+    algorithmic bytes from DRAM."""
+    return max(1, -(-6 * l2_bytes // cache_bytes) + 1)
+
+
 def sweep_time(fn, calls=1, burn_in=50, rounds=8):
     """Per-call GPU time of `fn` (which makes `calls` calls): at least
     `burn_in` calls first, then `rounds` timed rounds (CUDA events on the
@@ -685,7 +696,7 @@ def sweep_heads(kind, hq, hkv, n, dev, peaks, src):
         dq = q.to(dev)
         nbytes = 2 * n * hkv * D * 2 + 2 * hq * D * 2
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        copies = max(1, -(-2 * l2 // (nbytes - 2 * hq * D * 2)) + 1)
+        copies = rotation_copies(l2, nbytes - 2 * hq * D * 2)
         caches = [(kc.to(dev), vc.to(dev)) for _ in range(copies)]
         out = torch.empty_like(dq)
         calls = [lambda c=c: gqa.decode_heads(dq, c[0], c[1], out=out) for c in caches]
@@ -845,7 +856,7 @@ def run_sweep(args):
             q, kc, vc = decode_inputs(n, stress=stress)
             dq = q.to(dev)
             l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-            copies = max(1, -(-2 * l2 // (4 * kc.numel())) + 1)
+            copies = rotation_copies(l2, 4 * kc.numel())
             caches = [(kc.to(dev), vc.to(dev)) for _ in range(copies)]
             ws = torch.empty(gqa.decode_workspace_bytes(n), dtype=torch.uint8, device=dev)
             out = torch.empty_like(dq)

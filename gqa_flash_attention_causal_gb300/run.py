@@ -93,9 +93,11 @@ def main(argv=None):
         nbytes = 2.0 * L * 8 * 128 * 2 + 2 * 32 * 128 * 2
         line = f"decode L={L}: {ms * 1e3:.2f} us, {nbytes / ms / 1e6:.1f} GB/s"
         if args.graph:
-            # rotate through enough cache copies that they cannot stay in L2
+            # rotate through enough cache copies that they cannot stay in L2:
+            # the other copies stream 6x the L2 size between two reads of one
+            # (2x still left some launches reading part of their cache from L2)
             l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-            copies = max(1, -(-2 * l2 // (kc.numel() * 4)) + 1)
+            copies = max(1, -(-6 * l2 // (kc.numel() * 4)) + 1)
             caches = [(kc, vc)] + [(kc.clone(), vc.clone()) for _ in range(copies - 1)]
             ws = torch.empty(decode_workspace_bytes(L), dtype=torch.uint8, device=dev)
             calls = [lambda c=c: decode(q, c[0], c[1], out=out, workspace=ws) for c in caches]
