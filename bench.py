@@ -404,6 +404,50 @@ def run_ours(args, world, rank, local):
     # the timed region is ~0.1 s right after warm-up: the burst peak applies
     peak_tc = peaks["bf16_tflops"]
 
+    # ------------------------------------------------ sustained (seconds-long)
+    # The timed region above is ~0.1 s right after warm-up, i.e. a burst.  Here
+    # the same graphs run back to back for --sustain-s seconds; the last
+    # third is timed (CUDA events per kernel) with its own clock record and
+    # compared with the sustained bf16 peak.
+    sustained = None
+    if args.sustain_s > 0:
+        chunk = 10
+        t_end = time.time() + args.sustain_s * 2 / 3
+        while time.time() < t_end:
+            for _ in range(chunk):
+                g_pre.replay()
+                g_dec.replay()
+            torch.cuda.synchronize()
+        n_sus = max(chunk, int(args.sustain_s / 3 / (ms_step_local * 1e-3)))
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_sus)]
+        with ClockSampler(torch.cuda.current_device()) as sclk:
+            sclk.mark_start()
+            for i in range(n_sus):
+                evs[i][0].record(stream)
+                g_pre.replay()
+                evs[i][1].record(stream)
+                g_dec.replay()
+                evs[i][2].record(stream)
+                if i % chunk == chunk - 1:
+                    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            sclk.mark_stop()
+        s_total = evs[0][0].elapsed_time(evs[-1][2])
+        s_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+        s_pre_tf = prefill_flops(S_PREFILL) / (s_pre * 1e-3) / 1e12
+        sustained = {
+            "seconds_before_timing": round(args.sustain_s * 2 / 3, 2), "steps": n_sus,
+            "value": step_flops() * n_sus / (s_total * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": s_total / n_sus, "prefill_tflops": s_pre_tf,
+            "peak": peaks["bf16_tflops_sustained"], "peak_kind": f"bf16 sustained ({peaks_src})",
+            "frac": s_pre_tf / peaks["bf16_tflops_sustained"],
+            "decode_gbs": decode_bytes(L_DECODE) / (statistics.mean(
+                e[1].elapsed_time(e[2]) for e in evs) * 1e-3) / 1e9,
+            "clocks": sclk.summary(),
+        }
+        if gqa.device_error() != 0:
+            raise RuntimeError("device-side wait timed out in the sustained run")
+
     # ------------------------------------------------ end to end (host buffers)
     # Every step copies its own inputs from pinned host memory, runs the
     # prefill and the decode through the public API and copies both results
@@ -448,17 +492,22 @@ def run_ours(args, world, rank, local):
                 if done_compute[b] is not None:
                     s_h2d.wait_event(done_compute[b])  # buffers of step i-2 are free
                 m = [mark(s_h2d, i)]
-                for dst, src in zip(d_in[b], h_in[b]):
-                    dst.copy_(src, non_blocking=True)
+                # the prefill's inputs first, so that it can start before the
+                # decode's caches have arrived
+                ready = []
+                for first, last in ((0, 3), (3, 6)):
+                    for dst, src in zip(d_in[b][first:last], h_in[b][first:last]):
+                        dst.copy_(src, non_blocking=True)
+                    ready.append(torch.cuda.Event())
+                    ready[-1].record(s_h2d)
                 m.append(mark(s_h2d, i))
-                ready = torch.cuda.Event()
-                ready.record(s_h2d)
-            s_cmp.wait_event(ready)
+            s_cmp.wait_event(ready[0])
             if done_d2h[b] is not None:
                 s_cmp.wait_event(done_d2h[b])  # outputs of step i-2 are copied out
             m.append(mark(s_cmp, i))
             with torch.cuda.stream(s_cmp):
                 gqa.prefill(d_in[b][0], d_in[b][1], d_in[b][2], causal=True, out=d_out[b][0])
+                s_cmp.wait_event(ready[1])
                 gqa.decode(d_in[b][3], d_in[b][4], d_in[b][5], out=d_out[b][1])
             m.append(mark(s_cmp, i))
             done_compute[b] = torch.cuda.Event()
@@ -535,6 +584,7 @@ def run_ours(args, world, rank, local):
             "l2": "inputs larger than L2 (prefill q 256 MiB + k,v 128 MiB; decode KV 256 MiB)",
             "launch": "each step replays a CUDA graph of the prefill and one of the decode",
         },
+        "sustained": sustained,
         "roofline": {
             "kernel": "prefill_kernel",
             "bound": "tensor",
@@ -910,6 +960,8 @@ def main(argv=None):
     ap.add_argument("--ref-total", type=float, default=150.0,
                     help="CPU seconds the whole reference arm should take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps for the sustained figure (0: skip)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step, print one line per configuration of the "
                          "pages' Result table (time, throughput, roofline, parity)")
