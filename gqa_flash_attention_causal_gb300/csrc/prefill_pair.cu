@@ -3,18 +3,18 @@
 // two SMs of a cluster of two CTAs (cta_group::2).
 //
 // The chowfi/kernels README ("What helped most", item 2) reads K and V once
-// for every group of query rows that needs them.  Here the two CTAs of a pair
+// for all the query heads of a group.  Here the two CTAs of a pair work on
+// two query heads of the same KV group over the same 256 query rows, and
 // share each K/V tile: an MMA of M = 256 rows (128 in each CTA's tensor
 // memory) takes its B operand half from each CTA's shared memory, so a CTA
 // stages only half of every K tile (64 keys) and half of every V tile (64
 // dims), and its tensor core reads half the B bytes per FLOP that it reads in
 // the single-CTA kernel.
 //
-// Work item = one query head x 512 query rows.  Pair tile A is rows 0..255
-// of the item, pair tile B rows 256..511; CTA c holds rows 128c..128c+127 of
-// each pair tile as its Q tiles A and B.  Both CTAs visit the KV tiles of
-// the pair tile's later rows, so CTA 0 sees one fully masked tile at the end
-// of each pair tile in the causal case.
+// Work item = two query heads h0, h0 + 1 (one KV head) x 256 query rows,
+// CTA c taking head h0 + c as two 128-row Q tiles A and B -- exactly the
+// single-CTA kernel's item, so both CTAs mask the same causal diagonal and
+// walk the same KV tiles.  Needs an even number of query heads per KV head.
 //
 // Roles per CTA (384 threads, as in prefill.cu):
 //   warps 0-3 / 4-7  softmax of Q tile A / B (thread = TMEM lane = row)
@@ -60,7 +60,7 @@ constexpr int kStageBytes = kSoftmaxWarps * kStageWarpBytes;
 constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kStageBytes + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
-constexpr int kItemRows = 4 * kBM;  // query rows per work item
+constexpr int kItemRows = 2 * kBM;  // query rows per work item
 
 static_assert(kBM == kPrefillBoxRows && kBN / 2 == kPairKBoxRows, "tensor-map boxes");
 
@@ -82,26 +82,28 @@ struct Bars {
     __device__ uint32_t o_full(int t) const { return base + 48 + 16 * kStages + 8 * t; }
 };
 
-// Items (512-row block b, head h) of one sequence of S rows, dealt to the
-// pairs longest first (b descending when causal) in a snake order.
+// Items (256-row block b, head pair h0 = 2p, 2p + 1) of one sequence of S
+// rows, dealt to the CTA pairs longest first (b descending when causal) in a
+// snake order; the head pairs of one KV head are adjacent.
 struct PairWork {
-    int S, T, n_blocks, n_items, causal, hq;
-    __device__ PairWork(int S_, int causal_, int hq_) : S(S_), causal(causal_), hq(hq_) {
+    int S, T, n_blocks, n_items, causal, hp;
+    __device__ PairWork(int S_, int causal_, int hq) : S(S_), causal(causal_), hp(hq / 2) {
         T = (S + kBM - 1) / kBM;
         n_blocks = (S + kItemRows - 1) / kItemRows;
-        n_items = n_blocks * hq;
+        n_items = n_blocks * hp;
     }
     __device__ int item(int r, int p, int G) const {
         return r * G + ((r & 1) ? (G - 1 - p) : p);
     }
-    __device__ void resolve(int idx, int &b, int &h) const {
-        b = causal ? n_blocks - 1 - idx / hq : idx / hq;
-        h = idx % hq;
+    // block b and the pair's first query head h0
+    __device__ void resolve(int idx, int &b, int &h0) const {
+        b = causal ? n_blocks - 1 - idx / hp : idx / hp;
+        h0 = 2 * (idx % hp);
     }
-    // KV tiles of pair tile t of block b: up to the diagonal of its later rows
+    // KV tiles visited by Q tile t of block b (up to its diagonal)
     __device__ int n_kv(int b, int t) const {
         if (!causal) return T;
-        const int n = 4 * b + 2 * t + 2;
+        const int n = 2 * b + t + 1;
         return n < T ? n : T;
     }
 };
@@ -117,15 +119,13 @@ struct Abort {
     }
 };
 
-// Bounded waits (about one second, or until either CTA aborts).  Barriers
-// here can receive arrivals from the peer CTA, so the waits acquire at
-// cluster scope.
+// Bounded waits (about one second, or until either CTA aborts).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned *err,
                                           unsigned code, const Abort &ab) {
-    bool ok = mbar_try_wait_cluster(bar, parity);
+    bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
         const long long t0 = clock64();
-        while (!(ok = mbar_try_wait_cluster(bar, parity))) {
+        while (!(ok = mbar_try_wait(bar, parity))) {
             if (*ab.own || clock64() - t0 > kWaitLimitCycles) break;
         }
     }
@@ -138,9 +138,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigne
 }
 __device__ __forceinline__ bool lone_wait(uint32_t bar, uint32_t parity, unsigned *err,
                                           unsigned code, const Abort &ab) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait_cluster(bar, parity)) {
+    while (!mbar_try_wait(bar, parity)) {
         if (*ab.own || clock64() - t0 > kWaitLimitCycles) {
             atomicOr(err, code);
             ab.raise();
@@ -234,16 +234,16 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
             for (int r = 0, n = 0; ok; ++r) {
                 const int idx = work.item(r, pair, G);
                 if (idx >= work.n_items) break;
-                int b, h;
-                work.resolve(idx, b, h);
-                const int g = h / group;
+                int b, h0;
+                work.resolve(idx, b, h0);
+                const int h = h0 + int(rank), g = h0 / group;
                 if (n > 0 &&
                     !(ok = lone_wait(bars.q_empty(), (n - 1) & 1, err, kErrWaitEmpty, ab)))
                     break;
                 ++n;
                 mbar_arrive_expect_tx_cluster(c_q_full, kQBytes);
                 for (int t = 0; t < kTiles; ++t) {
-                    const int row = (4 * b + 2 * t + int(rank)) * kBM;
+                    const int row = (2 * b + t) * kBM;
                     const uint32_t dst = sQ + t * kTileBytes;
                     tma_load_3d_pair(dst, &qmap, c_q_full, 0, h, row, pol_q);
                     tma_load_3d_pair(dst + kQHalf, &qmap, c_q_full, 64, h, row, pol_q);
@@ -305,8 +305,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
             for (int r = 0, n = 0; ok; ++r) {
                 const int idx = work.item(r, pair, G);
                 if (idx >= work.n_items) break;
-                int b, h;
-                work.resolve(idx, b, h);
+                int b, h0;
+                work.resolve(idx, b, h0);
                 const int nA = work.n_kv(b, 0), nB = work.n_kv(b, 1);
                 if (!(ok = lone_wait(bars.q_full(), n & 1, err, kErrWaitFull, ab))) break;
                 ++n;
@@ -375,8 +375,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
             for (int r = 0; ok; ++r) {
                 const int idx = work.item(r, pair, G);
                 if (idx >= work.n_items) break;
-                int b, h;
-                work.resolve(idx, b, h);
+                int b, h0;
+                work.resolve(idx, b, h0);
                 const int nA = work.n_kv(b, 0), nB = work.n_kv(b, 1);
                 const int k0 = kv;
                 for (int j = 0; j < nB && ok; ++j) {
@@ -419,9 +419,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int rr = 0; ok; ++rr) {
             const int idx = work.item(rr, pair, G);
             if (idx >= work.n_items) break;
-            int b, h;
-            work.resolve(idx, b, h);
-            const int qt = 4 * b + 2 * t + int(rank);  // this CTA's 128-row tile
+            int b, h0;
+            work.resolve(idx, b, h0);
+            const int h = h0 + int(rank);
+            const int qt = 2 * b + t;  // this CTA's 128-row tile
             const int n = work.n_kv(b, t);
             const int row = qt * kBM + r;
             float m_run = -INFINITY, l = 0.f;
@@ -436,8 +437,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
                     tmem_ld32_max(s_tm + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c),
                                   part_max[c]);
                 tmem_wait_ld();
-                // keys kbase + c with c <= lim are visible to this row (lim < 0:
-                // none, the extra tile a CTA-0 row meets past its diagonal)
+                // keys kbase + c with c <= lim are visible to this row
                 const int kbase = j * kBN;
                 int lim = S - 1 - kbase;
                 if (causal && row - kbase < lim) lim = row - kbase;
@@ -603,7 +603,8 @@ cudaError_t launch_prefill_pair(const CUtensorMap &qmap, const CUtensorMap &kmap
         configured[dev] = r;
     });
     if ((e = configured[dev]) != cudaSuccess) return e;
-    const long long n_items = (long long)((S + kItemRows - 1) / kItemRows) * hq;
+    if ((hq / hkv) % 2 != 0) return cudaErrorInvalidValue;  // heads are paired within a group
+    const long long n_items = (long long)((S + kItemRows - 1) / kItemRows) * (hq / 2);
     const int pairs = n_items < max_pairs[dev] ? int(n_items) : max_pairs[dev];
     cfg.gridDim = dim3(2 * pairs);
     cfg.numAttrs = 2;

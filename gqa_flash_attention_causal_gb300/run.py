@@ -14,7 +14,7 @@ import statistics
 
 import torch
 
-from . import decode, decode_workspace_bytes, prefill
+from . import decode, decode_workspace_bytes, prefill, prefill_pair
 from .inputs import decode_inputs, prefill_inputs
 
 
@@ -70,6 +70,8 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--prefill", type=int, default=0, help="prompt length S (0 = skip)")
     ap.add_argument("--non-causal", action="store_true")
+    ap.add_argument("--pair", action="store_true",
+                    help="prefill with the paired-CTA kernel (gqa_attn_prefill_pair)")
     ap.add_argument("--decode", type=int, default=0, help="KV cache length L (0 = skip)")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--graph", type=int, default=0,
@@ -81,9 +83,10 @@ def main(argv=None):
         S = args.prefill
         q, k, v = (t.to(dev) for t in prefill_inputs(S))
         out = torch.empty_like(q)
-        ms = _time(lambda: prefill(q, k, v, causal=not args.non_causal, out=out), args.iters)
+        fn = prefill_pair if args.pair else prefill
+        ms = _time(lambda: fn(q, k, v, causal=not args.non_causal, out=out), args.iters)
         flops = (2.0 if not args.non_causal else 4.0) * S * S * 32 * 128
-        print(f"prefill S={S} causal={not args.non_causal}: {ms:.4f} ms, "
+        print(f"prefill{'_pair' if args.pair else ''} S={S} causal={not args.non_causal}: {ms:.4f} ms, "
               f"{flops / ms / 1e9:.1f} TFLOP/s")
     if args.decode:
         L = args.decode

@@ -118,13 +118,14 @@ gqa_status gqa_attn_prefill_heads(const void *q, const void *k, const void *v,
 /*
  * gqa_attn_prefill (and, with lse non-NULL, gqa_attn_prefill_lse) computed by
  * the paired-CTA kernel: the CTAs run as clusters of two on the two SMs of a
- * TPC, and every tcgen05 MMA spans both SMs' tensor memory (M = 256 rows,
- * 128 per CTA), each CTA staging half of every K and V tile, so that the
- * pair reads each K/V tile into shared memory once (chowfi/kernels README,
- * "What helped most", item 2: read K and V once for every group of rows that
- * needs them).  Same arguments, layouts, result and limits as
- * gqa_attn_prefill_lse with lse optional; the result agrees with
- * gqa_attn_prefill's up to the order of fp32 accumulation.
+ * TPC, the two CTAs of a pair compute two query heads of one KV group over
+ * the same rows, and every tcgen05 MMA spans both SMs' tensor memory
+ * (M = 256 rows, 128 per CTA), each CTA staging half of every K and V tile,
+ * so that the pair reads each K/V tile into shared memory once for both
+ * heads (chowfi/kernels README, "What helped most", item 2: read K and V once
+ * for the query heads of a group).  Same arguments, layouts, limits and
+ * result as gqa_attn_prefill_lse with lse optional (the same fp32
+ * accumulation order: the output is identical to gqa_attn_prefill's).
  */
 gqa_status gqa_attn_prefill_pair(const void *q, const void *k, const void *v,
                                  void *out, float *lse, int S, int causal,

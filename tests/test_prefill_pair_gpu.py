@@ -11,8 +11,8 @@ from tests.parity import assert_close, covered_tiles, poisoned, sample_rows, til
 
 pytestmark = pytest.mark.gpu
 
-# around the 128-row CTA tile, the 256-row pair tile and the 512-row item,
-# ragged tails, and the degenerate S=1
+# around the 128-row tile and the 256-row item, ragged tails, and the
+# degenerate S=1
 FULL = [1, 2, 127, 128, 129, 255, 256, 257, 300, 511, 512, 513, 1000]
 
 
@@ -39,8 +39,8 @@ def test_pair_noncausal_full(S):
 
 @pytest.mark.parametrize("S", [4096, 16384])
 def test_pair_causal_every_tile(S):
-    """The first, last and a random row of every 128-row tile: both CTAs'
-    halves of every pair tile of every item, all heads."""
+    """The first, last and a random row of every 128-row tile, all heads:
+    both CTAs (both heads of a pair) of every item."""
     (q, k, v), out = run(S)
     rows = sorted(set(sample_rows(S)) | set(tile_rows(S, seed=S + 1)))
     assert covered_tiles(rows, S) == S // 128
@@ -51,9 +51,9 @@ def test_pair_causal_every_tile(S):
 
 @pytest.mark.parametrize("S,causal", [(1000, True), (3001, True), (2048, False)])
 def test_pair_matches_single_cta_kernel(S, causal):
-    """Same rows, same KV tiles in the same order, same fp32 accumulation per
-    row: the paired kernel reproduces gqa_attn_prefill exactly (the extra,
-    fully masked tile a CTA-0 row meets adds zero weights)."""
+    """Each CTA of a pair computes one head of the single-CTA kernel's item:
+    same rows, same KV tiles in the same order, same fp32 accumulation per
+    row, so the paired kernel reproduces gqa_attn_prefill exactly."""
     q, k, v = (t.cuda() for t in prefill_inputs(S))
     a = gqa.prefill(q, k, v, causal=causal)
     b = gqa.prefill_pair(q, k, v, causal=causal)
