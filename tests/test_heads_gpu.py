@@ -8,7 +8,7 @@ import torch
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
 from gqa_flash_attention_causal_gb300.inputs import normal_bf16
-from tests.parity import assert_close, poisoned
+from tests.parity import assert_close, poisoned, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -63,7 +63,8 @@ def test_prefill_heads_packed_sampled(hq, hkv):
     assert gqa.device_error() == 0
     for s, n in enumerate(lens):
         a = int(cu[s])
-        rows = sorted({0, n - 1, n // 2, min(n - 1, 127), min(n - 1, 256)})
+        # every 128-row tile of every sequence, all heads
+        rows = sorted({0, n - 1, n // 2, min(n - 1, 127), min(n - 1, 256)} | set(tile_rows(n, s)))
         want = oracle.prefill_rows(q[a:a + n], k[a:a + n], v[a:a + n], rows, causal=True)
         assert_close(out[a:a + n][rows], want, what=f"packed {hq}/{hkv} seq {s}")
 
@@ -120,7 +121,7 @@ def test_prefill_heads_at_the_head_limit(hq, hkv, S):
     gqa.prefill_heads(q.cuda(), k.cuda(), v.cuda(), out=out)
     torch.cuda.synchronize()
     assert gqa.device_error() == 0
-    rows = [0, S // 2, S - 1]
+    rows = sorted({0, S // 2, S - 1} | set(tile_rows(S)))
     assert_close(out[0, rows], oracle.prefill_rows(q, k, v, rows), what=f"prefill {hq}/{hkv}")
 
 

@@ -6,7 +6,7 @@ import torch
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
 from gqa_flash_attention_causal_gb300.inputs import decode_inputs, prefill_inputs
-from tests.parity import assert_close, sample_rows
+from tests.parity import assert_close, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def test_prefill_lse_sampled_16k():
     q, k, v = prefill_inputs(S)
     _, lse = gqa.prefill(q.cuda(), k.cuda(), v.cuda(), return_lse=True)
     torch.cuda.synchronize()
-    rows = sample_rows(S)
+    rows = sorted(set(sample_rows(S)) | set(tile_rows(S, seed=9)))  # every 128-row tile
     _, want_lse = oracle.prefill_rows(q, k, v, rows, with_lse=True)
     _lse_close(lse[0].cpu().numpy().T[rows], want_lse, "prefill lse sampled")
 
