@@ -56,3 +56,25 @@ def test_explicit_stream_is_used():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, want)
+
+
+def test_prefill_pair_uses_current_stream():
+    """The paired-CTA prefill (a cluster launch) captures into a graph too;
+    its first call, which sets up the per-device launch attributes, runs
+    before the capture."""
+    q, k, v = (t.cuda() for t in prefill_inputs(1000))
+    out = torch.empty_like(q)
+    _capture_and_compare(lambda: gqa.prefill_pair(q, k, v, out=out), out)
+
+
+def test_prefill_pair_then_prefill_on_one_stream():
+    """A paired prefill followed by a single-CTA prefill on the same stream
+    (each a programmatic dependent of the one before): both outputs equal."""
+    q, k, v = (t.cuda() for t in prefill_inputs(2500))
+    a, b = torch.empty_like(q), torch.empty_like(q)
+    for _ in range(3):
+        gqa.prefill_pair(q, k, v, out=a)
+        gqa.prefill(q, k, v, out=b)
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    assert torch.equal(a, b)
