@@ -143,6 +143,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            int issued = 0;
             for (int it = 0; it < n_iter; ++it) {
                 const int s = it % kStages;
                 if (it >= kStages &&
@@ -155,7 +156,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                 tma_load_3d(dst + kHalfBytes, &kmap, full, 64, g, row, pol);
                 tma_load_3d(dst + kTileBytes, &vmap, full, 0, g, row, pol);
                 tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, full, 64, g, row, pol);
+                issued = it + 1;
             }
+            // No copy may still be landing in shared memory when the CTA
+            // exits: wait (bounded) for the stages this thread filled last.
+            // Normally the compute warps have waited for them already; after
+            // a wait that gave up, some may still be in flight.
+            for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it)
+                mbar_wait(full0 + 8 * (it % kStages), (it / kStages) & 1, err, kErrWaitFull);
         }
         return;  // the producer takes no part in the merge below
     }

@@ -74,8 +74,9 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsOther = 104;
 constexpr int kQBytes = kTiles * kTileBytes;
 constexpr int kRingBytes = kStages * kTileBytes;
-// q_full, q_empty, kv_full[4], kv_empty[4], s_full[2], p_full[2], o_full[2]
-constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles;
+// q_full, q_empty, kv_full[4], kv_empty[4], s_full[2], p_full[2], o_full[2],
+// drain
+constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles + 1;
 // epilogue staging: per softmax warp, 32 rows x 64 columns of bf16 output
 constexpr int kStageWarpBytes = 32 * 64 * 2;
 constexpr int kStageBytes = kSoftmaxWarps * kStageWarpBytes;
@@ -105,6 +106,8 @@ struct Bars {
     __device__ uint32_t s_full(int t) const { return base + 16 + 16 * kStages + 8 * t; }
     __device__ uint32_t p_full(int t) const { return base + 32 + 16 * kStages + 8 * t; }
     __device__ uint32_t o_full(int t) const { return base + 48 + 16 * kStages + 8 * t; }
+    // the MMA issuer's last commit: every MMA it issued has completed
+    __device__ uint32_t drain() const { return base + 64 + 16 * kStages; }
 };
 
 // Work decomposition shared by every role.  The batch is B packed
@@ -317,6 +320,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             mbar_init(bars.p_full(t), 4 + 1);  // the tile's softmax warps + ring warp
             mbar_init(bars.o_full(t), 1);
         }
+        mbar_init(bars.drain(), 1);
         *abort = 0;
         fence_barrier_init();
     }
@@ -365,9 +369,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         if (lane == 0) {
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            int kv = 0;
+            int kv = 0, n = 0;  // K/V tiles and Q pairs issued
             bool ok = true;
-            for (int r = 0, n = 0; ok; ++r) {
+            for (int r = 0; ok; ++r) {
                 const int idx = work.item(r, cta, G);
                 if (idx >= work.n_items) break;
                 Item it;
@@ -401,6 +405,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                     }
                 }
             }
+            // No copy may still be landing in shared memory when the CTA
+            // exits: wait (bounded, regardless of an abort) for the last Q
+            // tiles and K/V tiles this thread issued.  Normally they have all
+            // been consumed already; after a wait that gave up, some may still
+            // be in flight.
+            for (int i = kv > kStages ? kv - kStages : 0; i < kv; ++i)
+                mbar_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err, kErrWaitFull);
+            if (n > 0) mbar_wait(bars.q_full(), (n - 1) & 1, err, kErrWaitFull);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------ MMA issuer
@@ -721,6 +733,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     __syncthreads();
     if (warp == kWarpMma) {
         tc_fence_after();
+        // Normally every MMA has completed here (the epilogue waited for the
+        // last ones).  After a wait gave up, some may still be running: the
+        // issuing thread's commit tells when they are done, and tensor memory
+        // is freed only then.
+        if (*abort && lane == 0) {
+            umma_commit(bars.drain());
+            mbar_wait(bars.drain(), 0, err, kErrWaitMma);
+        }
+        __syncwarp();
         tmem_dealloc(tmem, kTmemCols);
     }
 }

@@ -53,11 +53,13 @@ constexpr int kRegsSoftmax = 200;
 constexpr int kRegsOther = 104;
 constexpr int kQBytes = kTiles * kTileBytes;
 constexpr int kRingBytes = kStages * kSlotBytes;
-// q_full, q_empty, kv_full[8], kv_empty[8], s_full[2], p_full[2], o_full[2]
-constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles;
+// q_full, q_empty, kv_full[8], kv_empty[8], s_full[2], p_full[2], o_full[2],
+// drain
+constexpr int kNumBars = 2 + 2 * kStages + 3 * kTiles + 1;
 constexpr int kStageWarpBytes = 32 * 64 * 2;
 constexpr int kStageBytes = kSoftmaxWarps * kStageWarpBytes;
-constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kStageBytes + kNumBars * 8 + 16;
+// + TMEM address, abort flag, the two producers' copy counts (leader's copy)
+constexpr size_t kSmemBytes = 1024 + kQBytes + kRingBytes + kStageBytes + kNumBars * 8 + 32;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kItemRows = 2 * kBM;  // query rows per work item
@@ -80,6 +82,8 @@ struct Bars {
     __device__ uint32_t s_full(int t) const { return base + 16 + 16 * kStages + 8 * t; }
     __device__ uint32_t p_full(int t) const { return base + 32 + 16 * kStages + 8 * t; }
     __device__ uint32_t o_full(int t) const { return base + 48 + 16 * kStages + 8 * t; }
+    // the MMA issuer's last commit: every MMA it issued has completed
+    __device__ uint32_t drain() const { return base + 64 + 16 * kStages; }
 };
 
 // Items (256-row block b, head pair h0 = 2p, 2p + 1) of one sequence of S
@@ -181,6 +185,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + kQBytes + kRingBytes + kStageBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_mem + kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // [K/V copies, Q copies] issued by CTA 0's and CTA 1's producers (read in CTA 0)
+    volatile uint32_t *copies = tmem_slot + 2;
     const Bars bars{smem_u32(bar_mem)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -199,6 +205,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
             mbar_init(bars.p_full(t), 2 * 4 + 1);  // both CTAs' softmax warps + ring warp
             mbar_init(bars.o_full(t), 1);
         }
+        mbar_init(bars.drain(), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -229,9 +236,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
             const uint32_t c_q_full = mapa_shared(bars.q_full(), 0);
-            int kv = 0;
+            int kv = 0, n = 0;  // K/V halves and Q pairs issued
             bool ok = true;
-            for (int r = 0, n = 0; ok; ++r) {
+            for (int r = 0; ok; ++r) {
                 const int idx = work.item(r, pair, G);
                 if (idx >= work.n_items) break;
                 int b, h0;
@@ -269,6 +276,11 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
                     }
                 }
             }
+            // CTA 0 drains both producers' copies at the end (they complete on
+            // its barriers): tell it how many this one issued.
+            const uint32_t c_copies = mapa_shared(smem_u32(const_cast<uint32_t *>(copies)), 0);
+            st_shared_cluster_u32(c_copies + 8 * rank, uint32_t(kv));
+            st_shared_cluster_u32(c_copies + 8 * rank + 4, uint32_t(n));
         } else if (warp == kWarpMma && leader && lane == 0) {
             // -------------------------------------------------- MMA issuer (pair)
             int kv = 0;
@@ -550,9 +562,45 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
     }
 
     // Neither CTA leaves (or frees the pair's tensor memory) while the other
-    // may still run MMAs on it or arrive on its barriers.
+    // may still run MMAs on it, arrive on its barriers, or have copies landing
+    // in its shared memory.  Both producers' copies complete on CTA 0's
+    // barriers: once both have stopped issuing (first cluster barrier), CTA 0
+    // supplies the arrival of any phase that only one producer joined (the
+    // other gave up first; the two issue the same sequence, and one can lead
+    // by at most a ring's worth of K/V halves and one Q pair) and waits,
+    // bounded, for every phase either issued that may not have completed.
     __syncwarp();
     tc_fence_before();
+    cluster_sync();
+    // Normally every MMA has completed here (the epilogues waited for the
+    // last ones).  After a wait gave up, some may still be running: the
+    // issuing thread's commit tells when they are done, and tensor memory is
+    // freed (below) only then.
+    if (leader && warp == kWarpMma && lane == 0 && *abort_flag) {
+        tc_fence_after();
+        umma_commit_pair(bars.drain());
+        mbar_wait(bars.drain(), 0, err, kErrWaitMma);
+    }
+    if (leader && warp == kWarpLoad && lane == 0) {
+        const int kv0 = int(copies[0]), n0 = int(copies[1]);
+        const int kv1 = int(copies[2]), n1 = int(copies[3]);
+        const int kv_lo = min(kv0, kv1), kv_hi = max(kv0, kv1);
+        const int n_lo = min(n0, n1), n_hi = max(n0, n1);
+        // phases both joined, then the lone ones (their slots' previous
+        // phases, both joined, are complete by then)
+        for (int i = kv_lo > kStages ? kv_lo - kStages : 0; i < kv_lo; ++i)
+            mbar_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err, kErrWaitFull);
+        if (n_lo > 0) mbar_wait(bars.q_full(), (n_lo - 1) & 1, err, kErrWaitFull);
+        for (int i = kv_lo; i < kv_hi; ++i) {
+            mbar_arrive(bars.kv_full(i % kStages));
+            mbar_wait(bars.kv_full(i % kStages), (i / kStages) & 1, err, kErrWaitFull);
+        }
+        for (int i = n_lo; i < n_hi; ++i) {
+            mbar_arrive(bars.q_full());
+            mbar_wait(bars.q_full(), i & 1, err, kErrWaitFull);
+        }
+    }
+    __syncwarp();
     cluster_sync();
     if (warp == kWarpMma) {
         tc_fence_after();
