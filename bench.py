@@ -538,8 +538,15 @@ def run_ours(args, world, rank, local):
     # (the first step's upload) and drain (the last step's download) weigh the same
     e2e_steps = max(2, args.steps)
     barrier(world)
-    timeline = []
-    e2e_ms_local = e2e_run(e2e_steps, True, timeline)
+    # Three pipelined runs, the median reported: the host link of this part
+    # occasionally drops to about a tenth of its rate for 50-100 ms (seen
+    # in per-copy event timelines: 640 MiB host-to-device taking 25-45 ms
+    # instead of 3.5), which a single run may or may not catch.
+    runs = []
+    for _ in range(3):
+        tl = []
+        runs.append((e2e_run(e2e_steps, True, tl), tl))
+    e2e_ms_local, timeline = sorted(runs, key=lambda r: r[0])[1]
     serial_ms_local = e2e_run(e2e_steps, False)
     e2e_ms, e2e_flops = aggregate(e2e_ms_local, step_flops(), world)
     e2e_value = e2e_flops / (e2e_ms * 1e-3) / 1e12
@@ -613,7 +620,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "how": "public API from pinned host buffers; copies of neighbouring steps "
-                       "overlap the kernels (two buffer sets, separate copy streams)",
+                       "overlap the kernels (two buffer sets, separate copy streams); median "
+                       "of three runs of as many steps as the device-timed region",
+                "runs_ms_per_step": [round(r[0], 4) for r in runs],
                 "serialized": {"value": serial_value, "ms_per_step": serial_ms_local},
                 "timeline": timeline_summary(timeline)},
         "gpu_launches": launches,
