@@ -15,7 +15,10 @@
 //
 // The work is HBM-bound (4 flops per byte), so the design goal is keeping
 // enough bytes in flight: K/V tiles stream through a 6-stage TMA ring (192 KB
-// in flight per SM), one CTA per SM.  The 16-key x 128-dim x head-group
+// in flight per SM), one CTA per SM, and each CTA starts its first six
+// stages on their way into L2 before it waits for the preceding kernel (a
+// programmatic dependent launch), so a call's stream overlaps the previous
+// kernel's tail.  The 16-key x 128-dim x head-group
 // products go through warp-level bf16 MMA (m16n8k16, the group's heads in
 // its 8 N columns; other head layouts take groups of up to 16 as two N
 // tiles) with fp32 accumulation: one ldmatrix + one MMA replaces 256 scalar
