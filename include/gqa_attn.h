@@ -126,6 +126,8 @@ gqa_status gqa_attn_prefill_heads(const void *q, const void *k, const void *v,
  * for the query heads of a group).  Same arguments, layouts, limits and
  * result as gqa_attn_prefill_lse with lse optional (the same fp32
  * accumulation order: the output is identical to gqa_attn_prefill's).
+ * A device that cannot hold one two-CTA cluster of this kernel gives
+ * GQA_ERR_CUDA and nothing is launched.
  */
 gqa_status gqa_attn_prefill_pair(const void *q, const void *k, const void *v,
                                  void *out, float *lse, int S, int causal,
