@@ -106,3 +106,41 @@ def test_decode_large_cache():
     must be computed in 64 bits."""
     (q, kc, vc), out = run(1 << 20)
     assert_close(out, oracle.decode(q, kc, vc), what="L=2^20")
+
+
+def test_decode_one_hot_at_l_2_25():
+    """L = 2^25: each cache spans 64 GiB (the entry accepts up to 2^26, whose
+    two caches alone would take 256 GiB of the device), too large for a host
+    copy for the oracle, so the check is a property that holds at any size.
+    Every key is zero except key j, which every query head matches with score
+    128 * 2.125^2 / sqrt(128) ~ 51, against ln L ~ 17: all but ~1e-15 of each
+    head's softmax weight falls on j, so each output head equals v[j] of its KV
+    head (query head h reads KV head h // 4) exactly in bf16.  V differs by
+    position, KV head and dimension, and every value is at least 2^-7 in
+    magnitude (an odd multiple of 1/128 before rounding), so reading a wrong
+    position or head, or truncating a 64-bit offset, changes the result.
+    j is tried near the start, past the 2^31-byte offset and in the last split."""
+    L = 1 << 25
+    torch.cuda.empty_cache()
+    kc = torch.zeros((1, L, 8, 128), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    g = torch.arange(8, device="cuda", dtype=torch.float32).view(1, 8, 1)
+    d = torch.arange(128, device="cuda", dtype=torch.float32).view(1, 1, 128)
+    step = 1 << 20
+    for r0 in range(0, L, step):
+        j = torch.arange(r0, r0 + step, device="cuda", dtype=torch.int64)
+        pos = ((j * 37) % 101 - 50).to(torch.float32).view(-1, 1, 1)
+        vc[0, r0:r0 + step] = ((8 * pos + 32 * g + 2 * d + 1) / 128).to(torch.bfloat16)
+    q = torch.full((1, 1, 32, 128), 2.125, dtype=torch.bfloat16, device="cuda")
+    try:
+        for jstar in (5, (1 << 24) + 12345, L - 3):
+            kc[0, jstar] = 2.125
+            out = gqa.decode(q, kc, vc)
+            torch.cuda.synchronize()
+            assert gqa.device_error() == 0
+            want = vc[0, jstar].repeat_interleave(4, dim=0)
+            assert torch.equal(out[0, 0], want), f"one-hot key {jstar}"
+            kc[0, jstar] = 0
+    finally:
+        del kc, vc
+        torch.cuda.empty_cache()

@@ -134,3 +134,24 @@ def test_prefill_causal_large_sampled():
     assert_close(out[0, rows], want, what=f"causal S={S} sampled")
     # every row was written (rows past the last item would stay NaN)
     assert bool(torch.isfinite(out[0, ::997].float()).all())
+
+
+def test_prefill_causal_max_length_sampled():
+    """S = 2^20, the largest length the entry accepts: q and out span 8 GiB
+    each and their element offsets pass 2^32.  Sampled rows cover both ends,
+    the middle and the tile and item boundaries of the last block."""
+    S = 1 << 20
+    q, k, v = prefill_inputs(S)
+    out = poisoned((1, S, 32, 128))
+    try:
+        gqa.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, out=out)
+        torch.cuda.synchronize()
+        assert gqa.device_error() == 0
+        rows = [0, 1, 255, 256, S // 2 - 1, S // 2, S - 257, S - 256, S - 129, S - 128, S - 2,
+                S - 1]
+        want = oracle.prefill_rows(q, k, v, rows, causal=True)
+        assert_close(out[0, rows], want, what=f"causal S={S} sampled")
+        assert bool(torch.isfinite(out).all()), "unwritten output rows"
+    finally:
+        del out
+        torch.cuda.empty_cache()
