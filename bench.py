@@ -652,15 +652,51 @@ def timeline_summary(tl):
             "steps": len(tl), "first_steps": tl[:3], "last_steps": tl[-2:]}
 
 
+def bf16_rne_bits(x):
+    """bf16 bit patterns of float64 values rounded to nearest, ties to even,
+    directly from float64 (no intermediate float32 rounding).  Normal range
+    only, which covers attention outputs of N(0,1) inputs; zeros stay zero."""
+    import numpy as np
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                       # x = m * 2^e, 0.5 <= |m| < 1
+    r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)   # 8 significant bits, half to even
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_ulp_distance(a_bits, b_bits):
+    """Distance in bf16 units in the last place between two arrays of bf16
+    bit patterns (adjacent representable values are 1 apart; +0 and -0 are
+    the same point)."""
+    import numpy as np
+    def order(b):
+        b = np.asarray(b, dtype=np.uint16).astype(np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(order(a_bits) - order(b_bits))
+
+
+def ulp_summary(got_bits, want):
+    """How far bf16 outputs are from the correctly rounded bf16 of the fp64
+    reference values: the fractions at 0, within 1 and within 4 ulp.  (No
+    maximum: an output near zero has a tiny ulp, so an absolute error well
+    inside the tolerance can be thousands of ulps there.)"""
+    d = bf16_ulp_distance(got_bits, bf16_rne_bits(want))
+    return {"exact": float((d == 0).mean()), "within_1": float((d <= 1).mean()),
+            "within_4": float((d <= 4).mean())}
+
+
 def timed_parity(oracle_last, out, dout):
     """Error of the timed region's outputs against the oracle rows the CPU
     baseline computed (evenly spaced prefill rows, all heads; the whole
     decode), with the tolerance of the parity tests: max-abs <= 2e-2 and
     mean-abs <= 2e-3 for these N(0,1) inputs."""
     import numpy as np
+    import torch
     rows, want_pre, want_dec = oracle_last
     got_pre = out[0, rows].double().numpy()
     got_dec = dout.double().numpy().reshape(want_dec.shape)
+    pre_bits = out[0, rows].contiguous().view(torch.int16).numpy().view(np.uint16)
+    dec_bits = dout.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(want_dec.shape)
     e_pre, e_dec = np.abs(got_pre - want_pre), np.abs(got_dec - want_dec)
     finite = bool(np.isfinite(got_pre).all() and np.isfinite(got_dec).all())
     ok = (finite and e_pre.max() <= 2e-2 and e_pre.mean() <= 2e-3
@@ -670,6 +706,10 @@ def timed_parity(oracle_last, out, dout):
                         "tiles": S_PREFILL // 128, "heads": HQ,
                         "max_abs": float(e_pre.max()), "mean_abs": float(e_pre.mean())},
             "decode": {"max_abs": float(e_dec.max()), "mean_abs": float(e_dec.mean())},
+            "ulp": {"prefill": ulp_summary(pre_bits, want_pre),
+                    "decode": ulp_summary(dec_bits, want_dec),
+                    "what": "distance of each bf16 output from the correctly rounded bf16 "
+                            "of the fp64 oracle value"},
             "what": "outputs of the timed region's last step vs the fp64 oracle rows of the "
                     "CPU baseline"}
 
@@ -901,6 +941,7 @@ def run_sweep(args):
             want = oracle.prefill_rows(q, k, v, rows, causal=causal)
             t_or = time.perf_counter() - t0
             got = out[0, rows].double().cpu().numpy()
+            got_bits = out[0, rows].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
             if causal:
                 sample_flops = sum(4.0 * HQ * D * (r + 1) for r in rows)
                 oracle_ms = 1e3 * t_or * (2.0 * HQ * D * n * (n + 1)) / sample_flops
@@ -935,6 +976,8 @@ def run_sweep(args):
             want = oracle.decode(q, kc, vc)
             oracle_ms = 1e3 * (time.perf_counter() - t0)
             got = out.double().cpu().numpy().reshape(want.shape)
+            got_bits = out.cpu().contiguous().view(torch.int16).numpy().view(
+                np.uint16).reshape(want.shape)
             tput = decode_bytes(n) / (ms * 1e-3) / 1e9
             line = {"workload": "decode", "L": n, "stress": stress, "ms": ms, "ms_p05": p05,
                     "ms_p95": p95, "gbs": tput,
@@ -950,6 +993,7 @@ def run_sweep(args):
         line.update({"max_abs_err": float(err.max()), "mean_abs_err": float(err.mean()),
                      "tolerance_scale": scale,
                      "parity_ok": bool(err.max() <= 2e-2 * scale and err.mean() <= 2e-3 * scale),
+                     "ulp": ulp_summary(got_bits, want),
                      "oracle_ms_est": oracle_ms, "oracle_cores": oracle.max_threads(),
                      "peaks": src})
         print(json.dumps(line), flush=True)

@@ -65,3 +65,38 @@ def test_rotation_copies_stream_six_l2_between_reuses():
         n = bench.rotation_copies(l2, cache)
         assert (n - 1) * cache >= 6 * l2 > (n - 2) * cache
     assert bench.rotation_copies(l2, 10 * l2) == 2
+
+
+def test_bf16_rounding_from_float64_is_nearest_even():
+    """bf16_rne_bits against the definition: representable values map to
+    themselves, a value between two neighbours goes to the nearer, and an
+    exact midpoint goes to the neighbour whose last mantissa bit is 0."""
+    bits = np.arange(0x3F00, 0x4100, dtype=np.uint16)  # [0.5, 8), both parities
+    a = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nxt = ((bits.astype(np.uint32) + 1) << 16).view(np.float32).astype(np.float64)
+    ulp = nxt - a
+    assert np.array_equal(bench.bf16_rne_bits(a), bits)
+    assert np.array_equal(bench.bf16_rne_bits(a + 0.3 * ulp), bits)
+    assert np.array_equal(bench.bf16_rne_bits(a + 0.7 * ulp), bits + 1)
+    even = np.where(bits % 2 == 0, bits, bits + 1).astype(np.uint16)
+    assert np.array_equal(bench.bf16_rne_bits(a + 0.5 * ulp), even)
+    assert np.array_equal(bench.bf16_rne_bits(-(a + 0.7 * ulp)), (bits + 1) | 0x8000)
+    assert bench.bf16_rne_bits(np.array([0.0]))[0] == 0
+
+
+def test_bf16_ulp_distance_orders_across_zero():
+    d = bench.bf16_ulp_distance
+    assert d(np.array([0x3F80]), np.array([0x3F81]))[0] == 1      # 1.0 and its neighbour
+    assert d(np.array([0x0000]), np.array([0x8000]))[0] == 0      # +0 and -0
+    assert d(np.array([0x0001]), np.array([0x8001]))[0] == 2      # +/- smallest step
+    assert d(np.array([0xBF80]), np.array([0xBF82]))[0] == 2      # -1.0 side
+
+
+def test_timed_parity_ulp_of_rounded_oracle(monkeypatch):
+    """Outputs that are the oracle rounded to bf16 sit at 0 ulp (torch rounds
+    through float32, which can differ from direct rounding only at ties)."""
+    monkeypatch.setattr(bench, "S_PREFILL", 256)
+    last, out, dout = _oracle_rows()
+    u = bench.timed_parity(last, out, dout)["ulp"]
+    for part in ("prefill", "decode"):
+        assert u[part]["within_1"] == 1.0 and u[part]["exact"] >= 0.999, u
