@@ -63,3 +63,13 @@ def tile_rows(S: int, seed: int = 0):
 def covered_tiles(rows, S: int) -> int:
     """Number of distinct 128-row query tiles that contain one of `rows`."""
     return len({r // TILE for r in rows if 0 <= r < S})
+
+
+def bf16_ulp_distance(a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    """Distance in bf16 units in the last place between two bf16 tensors of one
+    shape (neighbouring representable values are 1 apart; +0 and -0 coincide)."""
+    def order(x):
+        i = x.contiguous().view(torch.int16).to(torch.int32)
+        mag = i & 0x7FFF
+        return torch.where(i < 0, -mag, mag)
+    return (order(a) - order(b)).abs()

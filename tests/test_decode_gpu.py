@@ -6,7 +6,7 @@ import torch
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
 from gqa_flash_attention_causal_gb300.inputs import decode_inputs
-from tests.parity import assert_close, poisoned, tolerance_scale
+from tests.parity import assert_close, bf16_ulp_distance, poisoned, tolerance_scale
 
 pytestmark = pytest.mark.gpu
 
@@ -80,15 +80,19 @@ def test_decode_gqa_packing_identical_heads():
 
 
 def test_decode_constant_v():
+    """Every cached V row equal to c: each chunk's normalised partial is c
+    times sum(bf16(p)) / sum(p), within 2^-9 of c in relative terms, and the
+    log-sum-exp merge of such partials stays there, so every output element
+    is c or a bf16 neighbour of c."""
     L = 5000
     q, kc, _ = decode_inputs(L, stress=True)
-    const = torch.randn(1, 1, 8, 128).to(torch.bfloat16)
+    const = torch.randn(1, 1, 8, 128, generator=torch.Generator().manual_seed(9)).to(
+        torch.bfloat16)
     vc = const.expand(1, L, 8, 128).contiguous()
     out = gqa.decode(q.cuda(), kc.cuda(), vc.cuda())
     torch.cuda.synchronize()
     want = const.repeat_interleave(4, dim=2).view(1, 1, 32, 128)
-    d = (out.cpu().double() - want.double()).abs()
-    assert float(d.max()) <= 2e-2 * float(const.abs().max())
+    assert int(bf16_ulp_distance(out.cpu(), want).max()) <= 1
 
 
 def test_decode_deterministic():

@@ -5,9 +5,9 @@ import torch
 
 import gqa_flash_attention_causal_gb300 as gqa
 import oracle
-from gqa_flash_attention_causal_gb300.inputs import prefill_inputs
-from tests.parity import (assert_close, covered_tiles, poisoned, sample_rows, tile_rows,
-                          tolerance_scale)
+from gqa_flash_attention_causal_gb300.inputs import normal_bf16, prefill_inputs
+from tests.parity import (assert_close, bf16_ulp_distance, covered_tiles, poisoned, sample_rows,
+                          tile_rows, tolerance_scale)
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +63,22 @@ def test_causal_row0_is_v0_exactly():
     (q, k, v), out = run(1000, stress=True)
     want = v[0, 0].repeat_interleave(4, dim=0)
     assert torch.equal(out[0, 0].cpu(), want)
+
+
+def test_prefill_constant_v():
+    """Every V row of a KV head equal to one vector c: each output row is c
+    times sum(bf16(p)) / sum(p), within 2^-9 of c in relative terms (less than
+    half a bf16 ulp), so every output element is c or a bf16 neighbour of c.
+    Stress-scale q and k push scores to +-hundreds (rescales, masked keys)."""
+    S = 1000
+    q, k, _ = prefill_inputs(S, stress=True)
+    const = normal_bf16((1, 1, 8, 128), 9)
+    v = const.expand(1, S, 8, 128).contiguous()
+    out = gqa.prefill(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert gqa.device_error() == 0
+    want = const.repeat_interleave(4, dim=2).expand(1, S, 32, 128)
+    assert int(bf16_ulp_distance(out.cpu(), want).max()) <= 1
 
 
 def test_prefill_gqa_packing_identical_heads():
