@@ -100,3 +100,31 @@ def test_timed_parity_ulp_of_rounded_oracle(monkeypatch):
     u = bench.timed_parity(last, out, dout)["ulp"]
     for part in ("prefill", "decode"):
         assert u[part]["within_1"] == 1.0 and u[part]["exact"] >= 0.999, u
+
+
+def test_reference_arm_line_keeps_the_contract():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores, a short
+    bounded sample here) prints one JSON line with the reference arm's keys:
+    its own cpu_baseline and an e2e object with no host<->device bytes, both
+    carrying the line's value."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--ref-seconds", "0.2",
+                        "--ref-total", "2"], capture_output=True, text=True, timeout=300,
+                       cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["metric"] and d["config"]["workload"] and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
